@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of the shared-prefix one-pass decision hot path on GB300.
+
+One step = one pass of the whole path over one batch: the token-budget pack plan, the
+prefix-tail attention of every question's tail against the shared prefix (one attention layer)
+and the label readout with its temperature softmax.  Default workload: the long-document case
+(prefix 18432 tokens, 64 questions with tails U[64,256], 32/8 heads, d 128, hidden 2560,
+vocabulary 151936, 2-26 labels, T 0.7), synthetic and seeded.
+
+Prints one JSON line (rank 0).  `--impl reference` times the FP64 CPU oracle on the host cores
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "questions/sec and prefill tokens/sec at 1 GB300; % BF16 TC peak and % HBM BW"
+FLUSH_BYTES = 512 << 20  # written between timed steps: larger than the 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="18k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stress", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle sample")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def attention_flops(lengths: np.ndarray, P: int, Hq: int, d: int) -> float:
+    """Algorithmic FLOPs: QK^T and PV over every prefix key once per tail row, causal tail only."""
+    t = lengths.astype(np.float64)
+    return 4.0 * Hq * d * (t.sum() * P + (t * (t + 1) / 2).sum())
+
+
+def traffic_record(kernel_src: str, key: str):
+    """DRAM bytes per launch from a committed ncu summary, only if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[key]
+        with open(kernel_src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if rec.get("source_sha256") == sha:
+            return float(rec["bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", self.gpu_id], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5 and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(parts)
+                except Exception:
+                    pass
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def build_workload(name: str):
+    from shared_prefix_question_gb300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    lengths = wl.tail_lengths(w)                       # request order
+    slot_lengths = np.sort(lengths, kind="stable")     # the tails packed in the plan's slot order
+    ins = wl.attention_inputs(w, lengths=slot_lengths)
+    rd = wl.readout_inputs(w, rows=ins.rows, last_idx=np.zeros(w.n, dtype=np.int32))
+    return w, lengths, ins, rd
+
+
+def cpu_baseline(w, lengths, ins, rd, target_s: float, n_threads: int = 0):
+    """The oracle, as it stands, on a bounded sample: the plan over every question, the attention
+    of the first q questions' tails (every head, every row) and their label readout."""
+    from oracle import oracle
+    cores = n_threads or os.cpu_count()
+
+    def run(q):
+        t0 = time.perf_counter()
+        oracle.pack_plan(lengths, 32768, 0)
+        toks = np.concatenate([np.arange(ins.seq_start[b], ins.seq_start[b] + ins.seq_len[b]) for b in range(q)])
+        tok = np.repeat(toks, ins.Hq).astype(np.int32)
+        head = np.tile(np.arange(ins.Hq), len(toks)).astype(np.int32)
+        oracle.prefix_tail_attention(ins.q, ins.k_pre, ins.v_pre, ins.k_tail, ins.v_tail, ins.seq_start, ins.seq_len,
+                                     ins.P, ins.Hq, ins.Hkv, ins.d, select=(tok, head), n_threads=cores)
+        last = (ins.cu_seqlens[1:q + 1] - 1).astype(np.int32)
+        oracle.label_readout(rd.hidden, last, rd.unembed, rd.label_off[:q + 1], rd.label_ids[:rd.label_off[q]],
+                             rd.temperature)
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    q = int(max(1, min(w.n, target_s / max(t1, 1e-3))))
+    if q > 1:
+        tq = run(q)
+    else:
+        tq = t1
+    return {"value": q / tq, "unit": "questions/s", "cores": cores, "kind": "oracle",
+            "sample": f"{q} of {w.n} questions (all heads and tail rows; plan over all {w.n}), "
+                      f"{tq:.1f} s of FP64 CPU work"}, q, tq
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w, lengths, ins, rd = build_workload(args.workload)
+    from oracle import oracle
+    oracle.build()
+    cores = os.cpu_count()
+    # each step: the oracle on one question's tail (all heads), its readout and the whole plan
+    times = []
+    for i in range(args.warmup + args.steps):
+        b = i % w.n
+        t0 = time.perf_counter()
+        oracle.pack_plan(lengths, 32768, 0)
+        toks = np.arange(ins.seq_start[b], ins.seq_start[b] + ins.seq_len[b])
+        tok = np.repeat(toks, ins.Hq).astype(np.int32)
+        head = np.tile(np.arange(ins.Hq), len(toks)).astype(np.int32)
+        oracle.prefix_tail_attention(ins.q, ins.k_pre, ins.v_pre, ins.k_tail, ins.v_tail, ins.seq_start,
+                                     ins.seq_len, ins.P, ins.Hq, ins.Hkv, ins.d, select=(tok, head), n_threads=cores)
+        lo, hi = rd.label_off[b], rd.label_off[b + 1]
+        oracle.label_readout(rd.hidden, np.array([ins.cu_seqlens[b + 1] - 1], dtype=np.int32), rd.unembed,
+                             np.array([0, hi - lo], dtype=np.int32), rd.label_ids[lo:hi].copy(), rd.temperature)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times)
+    value = args.steps / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "questions/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.description}", "P": w.P, "questions": w.n,
+                       "sample_per_step": "one question's tail rows x all heads, its readout, the full plan"},
+            "cpu_baseline": {"value": value, "unit": "questions/s", "cores": cores, "kind": "oracle",
+                             "sample": "one question per step"},
+            "e2e": {"value": value, "unit": "questions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from shared_prefix_question_gb300 import blink, build
+    build.build()
+    hbm_peak, tc_peak, tc_sustained, peak_kind = peaks()
+
+    w, lengths, ins, rd = build_workload(args.workload)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    # ---- device-resident inputs
+    d_len = i32(lengths)
+    q, kt, vt = bf(ins.q), bf(ins.k_tail), bf(ins.v_tail)
+    kp, vp = (bf(ins.k_pre), bf(ins.v_pre)) if ins.P else (None, None)
+    hidden, W = bf(rd.hidden), bf(rd.unembed)
+    off, ids = i32(rd.label_off), i32(rd.label_ids)
+    n, sum_k = w.n, len(rd.label_ids)
+    max_tail = int(lengths.max())
+    plan = {k: torch.empty(n + (1 if k in ("fwd_slot_start", "cu_seqlens") else 0), dtype=torch.int32, device=dev)
+            for k in ("order", "slot_of", "fwd_of_slot", "fwd_slot_start", "fwd_width", "cu_seqlens", "last_varlen",
+                      "last_padded")}
+    plan["n_forwards_dev"] = torch.empty(1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    probs = torch.empty(sum_k, dtype=torch.float32, device=dev)
+    ws_a = blink.new_workspace(blink.attention_workspace_bytes(ins.rows, n, ins.P, ins.Hq, ins.Hkv, ins.d), dev)
+    ws_r = blink.new_workspace(blink.readout_workspace_bytes(n), dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        blink.blink_pack_plan(d_len, 32768, 0, out=plan)
+        if ev:
+            ev[1].record(stream)
+        blink.blink_prefix_tail_attention(q, kp, vp, kt, vt, plan["cu_seqlens"], B=n, P=ins.P, max_tail=max_tail,
+                                          out=out, ws=ws_a)
+        if ev:
+            ev[2].record(stream)
+        blink.blink_label_readout(hidden, plan["last_varlen"], W, off, ids, rd.temperature, probs=probs, ws=ws_r,
+                                  slot_of=plan["slot_of"])
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = blink.blink_read_device_status(ws_a)
+    st_r = blink.blink_read_device_status(ws_r)
+    if st != 0 or st_r != 0:
+        raise SystemExit(f"device status after warm-up: attention {st}, readout {st_r}")
+
+    # ---- timed region: K steps, L2 flushed before each, per-kernel events on the launching stream
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
+    if rank == 0:
+        sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        step(evs[k])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    read_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * n / (ms_per_step / 1000.0)
+    prefill_tokens = ins.P + int(lengths.sum())  # blink.py `_prefill_tokens`: the shared prefix counted once
+
+    # ---- roofline of the dominant kernel (attention: a dense contraction on the tensor cores)
+    flops = attention_flops(lengths, ins.P, ins.Hq, ins.d)
+    attn_mean = statistics.mean(attn_ms)
+    achieved = flops / (attn_mean / 1000.0) / 1e12
+    traffic = traffic_record(os.path.join(ROOT, "shared_prefix_question_gb300", "csrc", "attention.cu"),
+                             f"attention_{w.name}")
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": achieved / tc_peak, "traffic": traffic,
+                "kernel": "attention_kernel<128>", "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)",
+                "flops_per_launch": flops}
+
+    line = {"metric": METRIC, "value": value, "unit": "questions/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.description}", "P": ins.P, "questions": n,
+                       "tail_tokens": int(lengths.sum()), "Hq": ins.Hq, "Hkv": ins.Hkv, "d": ins.d, "H": w.H,
+                       "V": w.V, "labels": sum_k, "temperature": w.temperature, "budget": 32768,
+                       "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB write)",
+                       "parallelism": f"replicas x{world}, questions sharded, no collective in the step"},
+            "prefill_tokens_per_s": world * prefill_tokens / (ms_per_step / 1000.0),
+            "kernels_ms": {"plan": statistics.mean(plan_ms), "attention": attn_mean,
+                           "readout": statistics.mean(read_ms)},
+            "roofline": roofline, "gpu_launches": 3 * args.steps, "clocks": clocks}
+
+    # ---- readout on the stress input (HBM-bound at scale)
+    if not args.no_stress and rank == 0:
+        line["roofline_readout_stress"] = readout_stress(blink, dev, hbm_peak, peak_kind, flush, args)
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    if not args.no_e2e:
+        line["e2e"] = e2e(blink, dev, w, lengths, ins, rd, flush, args, world)
+
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, lengths, ins, rd, args.cpu_seconds)[0]
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def readout_stress(blink, dev, hbm_peak, peak_kind, flush, args):
+    import torch
+    from shared_prefix_question_gb300 import workloads as wl
+    w = wl.WORKLOADS["readout_stress"]
+    off, ids = wl.label_csr(w)
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    W = (torch.randn(w.V, w.H, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    hidden = torch.randn(w.n, w.H, generator=g, device=dev).to(torch.bfloat16)
+    last = torch.arange(w.n, dtype=torch.int32, device=dev)
+    d_off = torch.from_numpy(off).to(dev)
+    d_ids = torch.from_numpy(ids).to(dev)
+    probs = torch.empty(len(ids), dtype=torch.float32, device=dev)
+    ws = blink.new_workspace(blink.readout_workspace_bytes(w.n), dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        blink.blink_label_readout(hidden, last, W, d_off, d_ids, 1.0, probs=probs, ws=ws)
+    times = []
+    for _ in range(max(10, args.steps)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        blink.blink_label_readout(hidden, last, W, d_off, d_ids, 1.0, probs=probs, ws=ws)
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in times)
+    distinct = len(np.unique(ids))
+    nbytes = distinct * w.H * 2 + w.n * w.H * 2 + len(ids) * 4
+    achieved = nbytes / (ms / 1000.0) / 1e9
+    del W
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+            "traffic": None, "kernel": "readout_kernel", "ms": ms, "algorithmic_bytes": nbytes,
+            "input": f"512 questions, {len(ids)} labels ({distinct} distinct rows) drawn per question without "
+                     f"replacement from {w.V}, hidden {w.H}; includes the counter memset",
+            "peak_kind": f"{peak_kind} copy bandwidth"}
+
+
+def e2e(blink, dev, w, lengths, ins, rd, flush, args, world):
+    """Same step through the C ABI with HOST inputs: every step copies its inputs from pinned host
+    memory and reads the probabilities back (the readout's host-output path, one D2H copy)."""
+    import torch
+    import torch.distributed as dist
+
+    def pinned(a, dtype):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(dtype)).pin_memory()
+        return t
+
+    host = {"len": pinned(lengths.astype(np.int32), np.int32), "q": pinned(ins.q, np.int16),
+            "kt": pinned(ins.k_tail, np.int16), "vt": pinned(ins.v_tail, np.int16),
+            "hid": pinned(rd.hidden, np.int16), "off": pinned(rd.label_off, np.int32),
+            "ids": pinned(rd.label_ids, np.int32)}
+    if ins.P:
+        host["kp"] = pinned(ins.k_pre, np.int16)
+        host["vp"] = pinned(ins.v_pre, np.int16)
+    devb = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host.items()}
+    W = torch.from_numpy(np.ascontiguousarray(rd.unembed).view(np.int16)).view(torch.bfloat16).to(dev)  # resident
+    h_probs = torch.empty(len(rd.label_ids), dtype=torch.float32, pin_memory=True)
+    n = w.n
+    plan = None
+    out = torch.empty(ins.q.shape, dtype=torch.bfloat16, device=dev)
+    ws_a = blink.new_workspace(blink.attention_workspace_bytes(ins.rows, n, ins.P, ins.Hq, ins.Hkv, ins.d), dev)
+    ws_r = blink.new_workspace(blink.readout_workspace_bytes(n), dev)
+    bf = torch.bfloat16
+
+    def one():
+        nonlocal plan
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        plan = blink.blink_pack_plan(devb["len"], 32768, 0, out=plan)
+        blink.blink_prefix_tail_attention(devb["q"].view(bf), devb["kp"].view(bf) if ins.P else None,
+                                          devb["vp"].view(bf) if ins.P else None, devb["kt"].view(bf),
+                                          devb["vt"].view(bf), plan["cu_seqlens"], B=n, P=ins.P,
+                                          max_tail=int(lengths.max()), out=out, ws=ws_a)
+        blink.blink_label_readout(devb["hid"].view(bf), plan["last_varlen"], W, devb["off"], devb["ids"],
+                                  rd.temperature, host_probs=h_probs, ws=ws_r, slot_of=plan["slot_of"])
+
+    for _ in range(max(2, args.warmup)):
+        one()
+    times = []
+    steps = max(5, min(args.steps, 30))
+    if world > 1:
+        dist.barrier()
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        one()  # ends with the readout's synchronising host copy
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / steps
+    if world > 1:
+        t = torch.tensor([sec], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    return {"value": world * n / sec, "unit": "questions/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(h_probs.numel() * 4 + 4), "ms_per_step": sec * 1000, "steps": steps,
+            "resident": "unembedding (model weight) stays on the device"}
+
+
+if __name__ == "__main__":
+    main()

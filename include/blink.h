@@ -1,0 +1,181 @@
+/*
+ * blink.h -- C ABI of the GB300 (sm_103a) library for the shared-prefix one-pass decision path.
+ *
+ * Many questions share one prefix (a system prompt plus the evidence).  The prefix KV is held
+ * once in a contiguous arena; each question runs only its tail, which attends to the prefix
+ * without a mask and to its own tail causally.  The answer is read from the next-token
+ * distribution restricted to the offered option labels: the last-token hidden state against
+ * the unembedding rows of those labels, then a temperature softmax.  No tokens are generated.
+ *
+ * Sources (the pages this library restates):
+ *   blink.py   -- the "blink-4b" serving module: `_batches`, `_padded`, `_forward`,
+ *                 `_forward_shared`, `_read`, `_read_batched`, `softmax`, the limits
+ *                 MAX_OPTIONS / MAX_QUESTIONS / MAX_INPUT_TOKENS / TOKEN_BUDGET and the
+ *                 PREFIX_CACHE note;
+ *   engine.py  -- "simit" backends/mot: the contiguous KV arena and its varlen attention
+ *                 metadata (cu_seqlens, per-request region start, keys used).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named d_* and all tensor pointers are DEVICE pointers; h_* are HOST pointers
+ *     (pinned memory for asynchronous copies).  The caller owns every buffer; the library
+ *     allocates nothing and keeps no state between calls.
+ *   - bf16 tensors are passed as `blink_bf16` (16-bit storage of bfloat16 values), row-major.
+ *   - Calls are asynchronous on `stream` unless a host output is requested, in which case the
+ *     call synchronises the stream before returning.
+ *   - Arguments are checked on the host first (BLINK_INVALID_ARG / BLINK_OUT_OF_RANGE, nothing
+ *     launched).  Problems only visible on the device (a bad length or label id inside a
+ *     device array, a bounded wait that ran out) are latched in a device error word, read back
+ *     by the host-output path or by blink_read_device_status().  No kernel traps.
+ */
+#ifndef BLINK_H
+#define BLINK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t blink_bf16;
+typedef int32_t blink_status;
+
+#define BLINK_OK 0
+#define BLINK_INVALID_ARG 1          /* malformed argument (null pointer, bad shape, T <= 0 ...) */
+#define BLINK_OUT_OF_RANGE 2         /* a limit of the pages is exceeded (options, questions, context) */
+#define BLINK_WORKSPACE_TOO_SMALL 3  /* ws_bytes below what the *_workspace() query returned */
+#define BLINK_CUDA_ERROR 4           /* a CUDA runtime call failed; cudaGetLastError() has the detail */
+#define BLINK_DEVICE_FLAG 5          /* a device-side check failed (bad length, label id, CSR offsets) */
+#define BLINK_DEVICE_TIMEOUT 6       /* a bounded wait inside a kernel ran out; outputs are invalid */
+
+/* Limits from blink.py: MAX_OPTIONS, MAX_QUESTIONS, MAX_INPUT_TOKENS.  The planner also takes
+ * up to 64 requests of 512 questions at once (blink.py `Batcher.MAX_REQUESTS` packs every
+ * question of every request into the same forwards). */
+#define BLINK_MAX_OPTIONS 255
+#define BLINK_MAX_QUESTIONS 512
+#define BLINK_MAX_INPUT_TOKENS 131072
+#define BLINK_MAX_PLAN_SEQUENCES 32768
+
+/* A short English description of a status code (a static string). */
+const char *blink_status_string(blink_status s);
+
+/* Reads (and, if `clear` != 0, resets) the device error word at the start of a workspace
+ * passed to blink_prefix_tail_attention or blink_label_readout.  Synchronises `stream`.
+ * Returns BLINK_OK, BLINK_DEVICE_FLAG or BLINK_DEVICE_TIMEOUT (or BLINK_CUDA_ERROR). */
+blink_status blink_read_device_status(void *d_ws, int32_t clear, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Pack plan -- blink.py `_batches` (token-budget packing, shortest first, a forward closes when
+ * (longest x count) would pass the padded-token budget or at the row cap; a sequence longer
+ * than the budget runs alone) and `_padded` (right padding to each forward's longest).
+ *
+ * d_lengths [n]        sequence lengths (tails, or whole prompts on the plain path), 1..131072
+ * n                    1..BLINK_MAX_PLAN_SEQUENCES
+ * budget               padded tokens per forward (blink.py TOKEN_BUDGET = 32768), >= 1
+ * max_rows             row cap per forward, 0 = none (blink.py caps rows on the prefix path)
+ * Outputs (device, int32; slot s = the s-th sequence in the stable ascending length order):
+ *   d_order [n]            sequence index held by slot s
+ *   d_slot_of [n]          the inverse: slot holding sequence i (d_slot_of[d_order[s]] == s)
+ *   d_fwd_of_slot [n]      forward of slot s
+ *   d_fwd_slot_start [n+1] first slot of forward f for f <= n_forwards; n beyond
+ *   d_fwd_width [n]        padded width (longest length) of forward f; 0 beyond n_forwards
+ *   d_cu_seqlens [n+1]     varlen token offsets of the slots (cu[0] = 0)
+ *   d_last_varlen [n]      last token of slot s in the varlen packing: cu[s+1] - 1
+ *   d_last_padded [n]      last token of slot s in its forward's padded [rows, width] batch:
+ *                          row * width + len - 1
+ *   d_n_forwards [1]       number of forwards, or -1 if a length was outside 1..131072
+ *   h_n_forwards           optional (may be NULL): the same count copied to pinned host memory;
+ *                          when given, the call synchronises the stream.
+ * Errors: BLINK_INVALID_ARG (null output, budget < 1, max_rows < 0), BLINK_OUT_OF_RANGE (n),
+ * BLINK_DEVICE_FLAG (only with h_n_forwards: a length out of range), BLINK_CUDA_ERROR.
+ * The planner is one thread block; it uses no workspace.
+ * ------------------------------------------------------------------------------------------ */
+blink_status blink_pack_plan(const int32_t *d_lengths, int32_t n, int32_t budget, int32_t max_rows,
+                             int32_t *d_order, int32_t *d_slot_of, int32_t *d_fwd_of_slot, int32_t *d_fwd_slot_start,
+                             int32_t *d_fwd_width, int32_t *d_cu_seqlens, int32_t *d_last_varlen,
+                             int32_t *d_last_padded, int32_t *d_n_forwards, int32_t *h_n_forwards,
+                             cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Prefix-tail attention -- blink.py PREFIX_CACHE note and `_forward_shared` (the prefix is
+ * encoded once; every tail runs against it: same tokens, same positions, only the
+ * floating-point order differs), with the arena layout of simit engine.py.
+ *
+ * For question b, query head h (kv head h / (Hq/Hkv)) and tail row i:
+ *   O = softmax(scale * q . [K_pre ; K_tail_b[0..i]]^T) [V_pre ; V_tail_b[0..i]]
+ * i.e. every prefix key without a mask and the question's own tail causally.  The prefix part
+ * and the tail part are merged by log-sum-exp.
+ *
+ * q      [rows, Hq, d]   bf16; question b's tail at rows start_b .. start_b + len_b - 1
+ * k_pre  [P, Hkv, d]     bf16; position p's keys at k_pre + p * pre_row_stride (elements), so
+ * v_pre                  the prefix may be a region of a wider KV arena; pre_row_stride >= Hkv*d
+ *                        and a multiple of 8; 16-byte aligned base.  Unused when P == 0.
+ * k_tail, v_tail [rows, Hkv, d] bf16, same rows as q
+ * d_cu_seqlens [B+1]     len_b = cu[b+1] - cu[b]; in the varlen layout (d_seq_start == NULL)
+ *                        start_b = cu[b] - cu[0], so a slice of a larger cu array can be passed
+ *                        together with pointers offset by cu[0] rows
+ * d_seq_start [B]        right-padded layout: start_b, strictly increasing, rows not shared;
+ *                        rows owned by no question get O = 0 and LSE = -inf
+ * B                      1..BLINK_MAX_PLAN_SEQUENCES questions
+ * rows                   token rows of q / k_tail / v_tail / out (>= 1)
+ * P                      prefix length, 0 (plain causal path) .. 131072
+ * max_tail               upper bound of len_b, checked on the device; P + max_tail <= 131072
+ * Hq, Hkv, d             Hq % Hkv == 0, Hq/Hkv <= 128, d in {64, 128}
+ * scale                  softmax scale; <= 0 selects 1/sqrt(d)
+ * out   [rows, Hq, d]    bf16 (round to nearest even)
+ * lse   [Hq, rows]       optional (may be NULL): fp32 natural-log log-sum-exp of each row
+ * d_ws, ws_bytes         workspace of at least blink_attention_workspace(...) bytes, zero-filled
+ *                        before its first use; the first word is the device error word
+ * Errors: BLINK_INVALID_ARG, BLINK_OUT_OF_RANGE, BLINK_WORKSPACE_TOO_SMALL, BLINK_CUDA_ERROR;
+ * device-side: BLINK_DEVICE_FLAG (a length outside 1..max_tail or past `rows`),
+ * BLINK_DEVICE_TIMEOUT.
+ * ------------------------------------------------------------------------------------------ */
+size_t blink_attention_workspace(int32_t rows, int32_t B, int32_t P, int32_t Hq, int32_t Hkv, int32_t d);
+
+blink_status blink_prefix_tail_attention(const blink_bf16 *q, const blink_bf16 *k_pre, const blink_bf16 *v_pre,
+                                         int64_t pre_row_stride, const blink_bf16 *k_tail,
+                                         const blink_bf16 *v_tail, const int32_t *d_cu_seqlens,
+                                         const int32_t *d_seq_start, int32_t B, int32_t rows, int32_t P,
+                                         int32_t max_tail, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                                         blink_bf16 *out, float *lse, void *d_ws, size_t ws_bytes,
+                                         cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Label readout -- blink.py `_read` / `_read_batched` (the last hidden state of each question
+ * against the lm_head rows of its offered labels only, in FP32), `softmax` (z / T, minus the
+ * max, exp, normalise) and `decide` (the temperature must be positive).
+ *
+ * hidden [hidden_rows, H] bf16, row r at hidden + r * hidden_row_stride (elements; multiple of 8)
+ * d_last_idx              hidden row of each last token (0 <= idx < hidden_rows): indexed by
+ *                         question (d_slot_of == NULL) or by slot (question b reads
+ *                         d_last_idx[d_slot_of[b]]), so the plan's d_last_varlen / d_slot_of
+ *                         can be passed straight through
+ * unembed [V, H]          bf16 row-major; H a multiple of 8, 16-byte aligned
+ * d_label_off [B+1], d_label_ids [sum_k]  CSR, request order: question b offers
+ *                         label_ids[off[b] .. off[b+1]), 1..255 labels each, ids in [0, V)
+ * temperature             > 0 and finite
+ * d_probs [sum_k]         fp32 output probabilities (CSR like the ids)
+ * h_probs                 optional pinned host copy of d_probs; when given the call copies once
+ *                         and synchronises the stream, and reports device-side errors
+ * d_logits [sum_k]        optional fp32 raw logits (before the temperature)
+ * d_ws, ws_bytes          workspace of blink_label_readout_workspace(B) bytes, zero-filled before
+ *                         its first use; the call leaves its counters at zero
+ * A label id outside [0, V) makes that question's probabilities NaN and latches
+ * BLINK_DEVICE_FLAG; so do malformed offsets (then no probability is written).
+ * ------------------------------------------------------------------------------------------ */
+size_t blink_label_readout_workspace(int32_t B);
+
+blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hidden_row_stride, int32_t hidden_rows,
+                                 const int32_t *d_last_idx, const int32_t *d_slot_of, const blink_bf16 *unembed,
+                                 int32_t V, int32_t H,
+                                 const int32_t *d_label_off, const int32_t *d_label_ids, int32_t B,
+                                 int32_t sum_k, float temperature, float *d_probs, float *h_probs,
+                                 float *d_logits, void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BLINK_H */

@@ -1,0 +1,197 @@
+"""Thin Python binding of the C ABI in include/blink.h (libblink.so, built in-tree for sm_103a).
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels.  Torch
+tensors supply device memory and the current CUDA stream; outputs are allocated with torch when
+the caller does not pass them.  There is no CPU fallback: without the built library or a CUDA
+device every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libblink.so")
+
+BLINK_OK = 0
+BLINK_INVALID_ARG = 1
+BLINK_OUT_OF_RANGE = 2
+BLINK_WORKSPACE_TOO_SMALL = 3
+BLINK_CUDA_ERROR = 4
+BLINK_DEVICE_FLAG = 5
+BLINK_DEVICE_TIMEOUT = 6
+
+MAX_OPTIONS = 255
+MAX_QUESTIONS = 512
+MAX_INPUT_TOKENS = 131072
+MAX_PLAN_SEQUENCES = 32768
+
+
+class BlinkError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "blink_status_string": (ctypes.c_char_p, [_i32]),
+    "blink_read_device_status": (_i32, [_vp, _i32, _vp]),
+    "blink_pack_plan": (_i32, [_vp, _i32, _i32, _i32] + [_vp] * 10 + [_vp]),
+    "blink_attention_workspace": (_sz, [_i32] * 6),
+    "blink_prefix_tail_attention": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                           _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "blink_label_readout_workspace": (_sz, [_i32]),
+    "blink_label_readout": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
+                                   _vp, _sz, _vp]),
+}
+
+
+def lib():
+    """Load libblink.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() or "
+                               "python -m shared_prefix_question_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGNATURES)
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().blink_status_string(int(status)).decode()
+    except Exception:  # library not loadable: still give a readable message
+        return "status"
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: torch.cuda.Stream | None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors passed to the library must be contiguous CUDA tensors")
+
+
+def _check(status: int, what: str):
+    if status != BLINK_OK:
+        raise BlinkError(status, what)
+
+
+# ------------------------------------------------------------------------------------------------ plan
+def blink_pack_plan(lengths: torch.Tensor, budget: int, max_rows: int = 0, out: dict | None = None,
+                    sync: bool = False, stream=None) -> dict:
+    """Token-budget pack plan of int32 `lengths` (device).  Returns the plan tensors; with
+    sync=True also `n_forwards` as a Python int (one pinned D2H copy, synchronising)."""
+    _need_cuda(lengths)
+    if lengths.dtype != torch.int32:
+        raise ValueError("lengths must be int32")
+    n = lengths.numel()
+    dev = lengths.device
+    if out is None:
+        out = {k: torch.empty(n + (1 if k in ("fwd_slot_start", "cu_seqlens") else 0), dtype=torch.int32, device=dev)
+               for k in ("order", "slot_of", "fwd_of_slot", "fwd_slot_start", "fwd_width", "cu_seqlens",
+                         "last_varlen", "last_padded")}
+        out["n_forwards_dev"] = torch.empty(1, dtype=torch.int32, device=dev)
+    host = torch.empty(1, dtype=torch.int32, pin_memory=True) if sync else None
+    st = lib().blink_pack_plan(_ptr(lengths), n, int(budget), int(max_rows), _ptr(out["order"]),
+                               _ptr(out["slot_of"]), _ptr(out["fwd_of_slot"]), _ptr(out["fwd_slot_start"]), _ptr(out["fwd_width"]),
+                               _ptr(out["cu_seqlens"]), _ptr(out["last_varlen"]), _ptr(out["last_padded"]),
+                               _ptr(out["n_forwards_dev"]), _ptr(host), _stream(stream))
+    _check(st, "blink_pack_plan")
+    if sync:
+        out["n_forwards"] = int(host.item())
+    return out
+
+
+# ------------------------------------------------------------------------------------------------ attention
+def attention_workspace_bytes(rows, B, P, Hq, Hkv, d) -> int:
+    return int(lib().blink_attention_workspace(rows, B, P, Hq, Hkv, d))
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled device workspace (the first word is the device error word)."""
+    return torch.zeros(max(256, (nbytes + 255) // 256 * 256), dtype=torch.uint8, device=device)
+
+
+def blink_prefix_tail_attention(q, k_pre, v_pre, k_tail, v_tail, cu_seqlens, B: int, P: int, max_tail: int,
+                                seq_start=None, scale: float = 0.0, out=None, lse=None, want_lse: bool = False,
+                                ws=None, pre_row_stride: int | None = None, stream=None):
+    """q [rows, Hq, d], k_tail/v_tail [rows, Hkv, d], k_pre/v_pre [P, Hkv, d] (or rows of an arena with
+    `pre_row_stride` elements), all bf16 on the device.  Returns (out, lse, ws)."""
+    _need_cuda(q, k_tail, v_tail, cu_seqlens, seq_start)
+    rows, Hq, d = q.shape
+    Hkv = k_tail.shape[1]
+    if P > 0:
+        if pre_row_stride is None:
+            _need_cuda(k_pre, v_pre)
+            pre_row_stride = Hkv * d
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(Hq, rows, dtype=torch.float32, device=q.device)
+    need = attention_workspace_bytes(rows, B, P, Hq, Hkv, d)
+    if ws is None:
+        ws = new_workspace(need, q.device)
+    st = lib().blink_prefix_tail_attention(
+        _ptr(q), _ptr(k_pre) if P > 0 else None, _ptr(v_pre) if P > 0 else None, int(pre_row_stride or 0),
+        _ptr(k_tail), _ptr(v_tail), _ptr(cu_seqlens), _ptr(seq_start), int(B), int(rows), int(P), int(max_tail),
+        int(Hq), int(Hkv), int(d), float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "blink_prefix_tail_attention")
+    return out, lse, ws
+
+
+def blink_read_device_status(ws: torch.Tensor, clear: bool = True, stream=None) -> int:
+    return int(lib().blink_read_device_status(_ptr(ws), 1 if clear else 0, _stream(stream)))
+
+
+# ------------------------------------------------------------------------------------------------ readout
+def readout_workspace_bytes(B: int) -> int:
+    return int(lib().blink_label_readout_workspace(B))
+
+
+def blink_label_readout(hidden, last_idx, unembed, label_off, label_ids, temperature: float, probs=None,
+                        host_probs=None, logits=None, ws=None, slot_of=None, stream=None):
+    """hidden [rows, H] bf16, last_idx int32 (per question, or per slot with `slot_of`), unembed [V, H]
+    bf16, CSR label_off [B+1] / label_ids [sum K] int32, all on the device.  Returns (probs, ws); if
+    `host_probs` (pinned fp32) is given the call copies into it and synchronises."""
+    _need_cuda(hidden, last_idx, unembed, label_off, label_ids, probs, logits, slot_of)
+    rows, H = hidden.shape
+    V = unembed.shape[0]
+    B = label_off.numel() - 1
+    sum_k = label_ids.numel()
+    if probs is None:
+        probs = torch.empty(sum_k, dtype=torch.float32, device=hidden.device)
+    if ws is None:
+        ws = new_workspace(readout_workspace_bytes(B), hidden.device)
+    st = lib().blink_label_readout(_ptr(hidden), int(hidden.stride(0)), int(rows), _ptr(last_idx), _ptr(slot_of), _ptr(unembed),
+                                   int(V), int(H), _ptr(label_off), _ptr(label_ids), int(B), int(sum_k),
+                                   float(temperature), _ptr(probs), _ptr(host_probs), _ptr(logits), _ptr(ws),
+                                   ws.numel(), _stream(stream))
+    _check(st, "blink_label_readout")
+    return probs, ws

@@ -1,0 +1,542 @@
+// attention.cu -- prefix-tail attention on tcgen05 tensor cores (blink.py PREFIX_CACHE note and
+// `_forward_shared`: every tail runs against the one shared prefix KV, same tokens and positions).
+//
+// Work decomposition.  Rows of the M dimension are (tail token, query head of one GQA group):
+// a 128-row tile holds tpt = 128 / g consecutive tokens times the g query heads that share one
+// kv head, so every K/V tile staged in shared memory serves all g heads.  A thread block owns
+// two such tiles (256 rows) of one kv head and sweeps the KV sequence:
+//   - the prefix tiles (all P prefix keys, no mask: every tail row sees every prefix key), then
+//   - the tail tiles: keys from the first question touched by the block up to its last token,
+//     masked per row to its own question (key >= question start) and causally (key <= token).
+// The running (max, sum) online softmax merges the parts: each new KV tile is folded into the
+// accumulator by log-sum-exp rescaling, which is exactly the LSE merge of the prefix and tail
+// partial results.
+//
+// Roles (320 threads):
+//   warp 8       TMA producer: Q tiles once, then K/V tiles into a ring of 4 shared-memory slots;
+//   warp 9       MMA issuer (one thread): S_t = Q_t K^T into tensor memory, O_t += P_t V with P_t
+//                read straight from tensor memory;
+//   warps 0-3/4-7 softmax for tile 0 / tile 1, one row per thread: reads S from tensor memory,
+//                masks, keeps (m, l), writes P (bf16) over S, rescales O lazily (only when the
+//                row max grew by more than 2^8), and finally normalises O and stores it.
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// MMA issue order: S0(i), PV1(i-1), S1(i), PV0(i), so each softmax warpgroup works while the
+// tensor core runs the other tile's products.
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace blink {
+namespace {
+
+constexpr int BM = 128;       // rows per M tile
+constexpr int BN = 128;       // keys per KV tile
+constexpr int kSlots = 4;     // K/V ring slots
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 bytes: one 64-column swizzle panel
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr uint32_t kTmemCols = 512;
+
+struct AttnArgs {
+    const int32_t *cu;         // [B+1]
+    const int32_t *seq_start;  // [B] or nullptr (varlen)
+    uint16_t *out;             // [rows, Hq, D]
+    float *lse;                // [Hq, rows] or nullptr
+    int *err;
+    int rows, B, P, Hq, Hkv, g, tpt, n_pre, max_tail;
+    float scale_log2;
+};
+
+template <int D>
+struct Layout {
+    static constexpr int kQTileBytes = BM * D * 2;
+    static constexpr int kKVTileBytes = BN * D * 2;
+    static constexpr int kPanels = D / 64;
+    static constexpr int kQOff0 = 0;
+    static constexpr int kQOff1 = kQTileBytes;
+    static constexpr int kKVOff = 2 * kQTileBytes;
+    static constexpr int kBarOff = kKVOff + kSlots * kKVTileBytes;
+    static constexpr int kBytes = kBarOff + 256;
+    static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
+};
+
+__device__ __forceinline__ int start_of(const AttnArgs &a, int b)
+{
+    return a.seq_start ? __ldg(a.seq_start + b) : __ldg(a.cu + b) - __ldg(a.cu);
+}
+__device__ __forceinline__ int len_of(const AttnArgs &a, int b) { return __ldg(a.cu + b + 1) - __ldg(a.cu + b); }
+
+// Largest b with start_b <= t, or -1.
+__device__ __forceinline__ int owner_floor(const AttnArgs &a, int t)
+{
+    int lo = 0, hi = a.B - 1, ans = -1;
+    while (lo <= hi) {
+        int mid = (lo + hi) >> 1;
+        if (start_of(a, mid) <= t) {
+            ans = mid;
+            lo = mid + 1;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    return ans;
+}
+
+__device__ __forceinline__ bool question_ok(const AttnArgs &a, int s, int L)
+{
+    return L >= 1 && L <= a.max_tail && s >= 0 && static_cast<long long>(s) + L <= a.rows;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kpre,
+                     const __grid_constant__ CUtensorMap tm_vpre, const __grid_constant__ CUtensorMap tm_ktail,
+                     const __grid_constant__ CUtensorMap tm_vtail, const AttnArgs a)
+{
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *q_s0 = base + L::kQOff0;
+    uint8_t *q_s1 = base + L::kQOff1;
+    uint8_t *kv_s = base + L::kKVOff;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + L::kBarOff);
+    uint64_t *q_full = bars + 0;
+    uint64_t *full = bars + 1;     // [4]
+    uint64_t *empty = bars + 5;    // [4]
+    uint64_t *s_full = bars + 9;   // [2]
+    uint64_t *p_full = bars + 11;  // [2]
+    uint64_t *o_full = bars + 13;  // [2]
+    uint64_t *mma_done = bars + 15;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 16);
+    int *sched = reinterpret_cast<int *>(tmem_holder + 1);  // kbeg, n_tail, abort
+    volatile int *abort_flag = sched + 2;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int head = blockIdx.y;
+    const int t0 = blockIdx.x * 2 * a.tpt;
+
+    if (threadIdx.x == kProducerWarp * 32) {
+        ptx::mbar_init(q_full, 1);
+        for (int i = 0; i < kSlots; ++i) {
+            ptx::mbar_init(full + i, 1);
+            ptx::mbar_init(empty + i, 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(s_full + t, 1);
+            ptx::mbar_init(p_full + t, 128);
+            ptx::mbar_init(o_full + t, 1);
+        }
+        ptx::mbar_init(mma_done, 1);
+        ptx::fence_mbar_init();
+        // Tail keys this block needs: from the start of the first question it touches.
+        const int t_end = min(t0 + 2 * a.tpt, a.rows);
+        int kbeg = -1;
+        int b = owner_floor(a, t0);
+        if (b >= 0) {
+            const int s = start_of(a, b), len = len_of(a, b);
+            if (!question_ok(a, s, len)) atomicCAS(a.err, 0, BLINK_DEVICE_FLAG);
+            else if (t0 < s + len) kbeg = s;
+        }
+        if (kbeg < 0 && b + 1 < a.B) {
+            const int s = start_of(a, b + 1);
+            if (s >= 0 && s < t_end) kbeg = s;
+        }
+        int n_tail = 0;
+        if (kbeg >= 0 && kbeg < t_end) n_tail = (t_end - kbeg + BN - 1) / BN;
+        sched[0] = kbeg < 0 ? 0 : kbeg;
+        sched[1] = n_tail;
+        sched[2] = 0;
+        ptx::tma_prefetch_desc(&tm_q);
+        ptx::tma_prefetch_desc(&tm_kpre);
+        ptx::tma_prefetch_desc(&tm_vpre);
+        ptx::tma_prefetch_desc(&tm_ktail);
+        ptx::tma_prefetch_desc(&tm_vtail);
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(tmem_holder, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    // Rows of a Q tile past g * tpt are never loaded: zero them so they stay finite.
+    const int rows_used = a.g * a.tpt;
+    if (warp < 8 && rows_used < BM) {
+        const int pad_bytes = (BM - rows_used) * 128;
+        for (int t = 0; t < 2; ++t) {
+            uint8_t *q = t == 0 ? q_s0 : q_s1;
+            for (int p = 0; p < L::kPanels; ++p) {
+                uint8_t *dst = q + p * kHalfBytes + rows_used * 128;
+                for (int off = threadIdx.x * 16; off < pad_bytes; off += 256 * 16)
+                    *reinterpret_cast<uint4 *>(dst + off) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    const uint32_t tmem = *tmem_holder;
+    const int kbeg = sched[0];
+    const int n_iter = a.n_pre + sched[1];
+
+    if (warp == kProducerWarp) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint32_t q_box = 64u * a.g * a.tpt * 2u;
+            // The second tile is loaded only if it starts inside the tensor (its rows past the end
+            // are then zero-filled by the copy); otherwise its rows stay as they are and are never
+            // stored.
+            const int q_tiles = (t0 + a.tpt < a.rows) ? 2 : 1;
+            int n = 0;
+            ptx::mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(q_tiles) * L::kPanels * q_box);
+            for (int t = 0; t < q_tiles; ++t)
+                for (int p = 0; p < L::kPanels; ++p)
+                    ptx::tma_load_3d((t == 0 ? q_s0 : q_s1) + p * kHalfBytes, &tm_q, p * 64, head * a.g,
+                                     t0 + t * a.tpt, q_full);
+            for (int it = 0; it < n_iter; ++it) {
+                const bool pre = it < a.n_pre;
+                const int kb = pre ? it * BN : kbeg + (it - a.n_pre) * BN;
+                bool ok = true;
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int slot = n % kSlots;
+                    const uint32_t ph = (n / kSlots) & 1;
+                    if (!ptx::mbar_wait(empty + slot, ph ^ 1u, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full + slot, L::kKVTileBytes);
+                    const CUtensorMap *map = pre ? (kv ? &tm_vpre : &tm_kpre) : (kv ? &tm_vtail : &tm_ktail);
+                    for (int p = 0; p < L::kPanels; ++p)
+                        ptx::tma_load_3d(kv_s + slot * L::kKVTileBytes + p * kHalfBytes, map, p * 64, head, kb,
+                                         full + slot);
+                    ++n;
+                }
+                if (!ok) break;
+            }
+            // Drain: every copy issued must have landed before the block may exit.
+            volatile int no_abort = 0;
+            ptx::mbar_wait(q_full, 0, &no_abort, a.err, BLINK_DEVICE_TIMEOUT);
+            for (int j = n > kSlots ? n - kSlots : 0; j < n; ++j) {
+                no_abort = 0;
+                ptx::mbar_wait(full + (j % kSlots), (j / kSlots) & 1, &no_abort, a.err, BLINK_DEVICE_TIMEOUT);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, true);
+            const uint32_t s_col[2] = {0u, 128u};
+            const uint32_t o_col[2] = {256u, 256u + D};
+            const uint32_t q_addr[2] = {ptx::smem_u32(q_s0), ptx::smem_u32(q_s1)};
+            const uint32_t kv_addr = ptx::smem_u32(kv_s);
+            auto qk = [&](int t, uint32_t k_addr) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + s_col[t], ptx::smem_desc_sw128(q_addr[t] + off, 16, 1024),
+                                ptx::smem_desc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto pv = [&](int t, uint32_t v_addr, bool first) {
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    ptx::mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8,
+                                ptx::smem_desc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                                (!first || kk > 0) ? 1u : 0u);
+            };
+            bool ok = ptx::mbar_wait(q_full, 0, abort_flag, a.err, BLINK_DEVICE_TIMEOUT);
+            ptx::tc_fence_after();
+            for (int i = 0; ok && i < n_iter; ++i) {
+                const int kslot = (2 * i) % kSlots, vslot = (2 * i + 1) % kSlots;
+                const uint32_t kph = ((2 * i) / kSlots) & 1, vph = ((2 * i + 1) / kSlots) & 1;
+                if (!(ok = ptx::mbar_wait(full + kslot, kph, abort_flag, a.err, BLINK_DEVICE_TIMEOUT))) break;
+                ptx::tc_fence_after();
+                const uint32_t k_addr = kv_addr + kslot * L::kKVTileBytes;
+                qk(0, k_addr);
+                ptx::mma_commit(s_full + 0);
+                if (i > 0) {
+                    const int pvslot = (2 * (i - 1) + 1) % kSlots;
+                    if (!(ok = ptx::mbar_wait(p_full + 1, (i - 1) & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)))
+                        break;
+                    ptx::tc_fence_after();
+                    pv(1, kv_addr + pvslot * L::kKVTileBytes, i - 1 == 0);
+                    ptx::mma_commit(empty + pvslot);
+                }
+                qk(1, k_addr);
+                ptx::mma_commit(s_full + 1);
+                ptx::mma_commit(empty + kslot);
+                if (!(ok = ptx::mbar_wait(p_full + 0, i & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT))) break;
+                if (!(ok = ptx::mbar_wait(full + vslot, vph, abort_flag, a.err, BLINK_DEVICE_TIMEOUT))) break;
+                ptx::tc_fence_after();
+                pv(0, kv_addr + vslot * L::kKVTileBytes, i == 0);
+                if (i == n_iter - 1) ptx::mma_commit(o_full + 0);
+            }
+            if (ok) {
+                if (n_iter > 0) {
+                    const int i = n_iter - 1;
+                    const int vslot = (2 * i + 1) % kSlots;
+                    if (ptx::mbar_wait(p_full + 1, i & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)) {
+                        ptx::tc_fence_after();
+                        pv(1, kv_addr + vslot * L::kKVTileBytes, i == 0);
+                        ptx::mma_commit(empty + vslot);
+                        ptx::mma_commit(o_full + 1);
+                    }
+                } else {
+                    ptx::mma_commit(o_full + 0);
+                    ptx::mma_commit(o_full + 1);
+                }
+            }
+            // Every MMA issued must be complete before tensor memory is released.
+            ptx::mma_commit(mma_done);
+            volatile int no_abort = 0;
+            ptx::mbar_wait(mma_done, 0, &no_abort, a.err, BLINK_DEVICE_TIMEOUT);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax (one row per thread)
+        const int t = warp >> 2;              // which of the two M tiles
+        const int r = (warp & 3) * 32 + lane;  // row inside the tile = TMEM lane
+        const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t s_col = t * 128u;
+        const uint32_t o_col = 256u + t * D;
+        const int tok = t0 + t * a.tpt + r / a.g;
+        const int hq = head * a.g + r % a.g;
+        const bool row_ok = r < rows_used && tok < a.rows;
+        bool owned = false;
+        int q_lo = 0;
+        if (row_ok) {
+            const int b = owner_floor(a, tok);
+            if (b >= 0) {
+                const int s = start_of(a, b), len = len_of(a, b);
+                if (!question_ok(a, s, len)) {
+                    atomicCAS(a.err, 0, BLINK_DEVICE_FLAG);
+                } else if (tok < s + len) {
+                    owned = true;
+                    q_lo = s;
+                }
+            }
+        }
+        const float sl2 = a.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int i = 0; i < n_iter; ++i) {
+            if (!(ok = ptx::mbar_wait(s_full + t, i & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT))) break;
+            ptx::tc_fence_after();
+            float s[BN];
+            {
+                uint32_t raw[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+                    ptx::tmem_ld32(trow + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(raw + c * 32));
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < BN; ++j) s[j] = __uint_as_float(raw[j]);
+            }
+            // masks
+            if (i < a.n_pre) {
+                const int kb = i * BN;
+                if (kb + BN > a.P) {
+                    const int lim = a.P - kb;
+#pragma unroll
+                    for (int j = 0; j < BN; ++j)
+                        if (j >= lim) s[j] = -INFINITY;
+                }
+            } else {
+                const int kb = kbeg + (i - a.n_pre) * BN;
+                const int lo_j = q_lo - kb;
+                const int hi_j = owned ? tok - kb : -1;
+#pragma unroll
+                for (int j = 0; j < BN; ++j)
+                    if (j < lo_j || j > hi_j) s[j] = -INFINITY;
+            }
+            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+            for (int j = 4; j < BN; j += 4) {
+                mx0 = fmaxf(mx0, s[j]);
+                mx1 = fmaxf(mx1, s[j + 1]);
+                mx2 = fmaxf(mx2, s[j + 2]);
+                mx3 = fmaxf(mx3, s[j + 3]);
+            }
+            const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+            const bool need = m_new > m + kRescaleThreshold;
+            const bool rescale = __any_sync(0xFFFFFFFFu, need);  // warp-uniform: TMEM access is collective
+            float alpha = 1.f;
+            if (rescale) {
+                alpha = (m == -INFINITY) ? 0.f : ptx::ex2(m - m_new);
+                l *= alpha;
+                m = m_new;
+            }
+            const float m_use = (m == -INFINITY) ? 0.f : m;
+            float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = ptx::ex2(fmaf(s[c * 64 + 2 * j], sl2, -m_use));
+                    const float p1 = ptx::ex2(fmaf(s[c * 64 + 2 * j + 1], sl2, -m_use));
+                    rs0 += p0;
+                    rs1 += p1;
+                    pk[j] = ptx::pack_bf16x2(p0, p1);
+                }
+                ptx::tmem_st32(trow + s_col + c * 32, pk);
+            }
+            l += rs0 + rs1;
+            // O_t still holds the sum up to the previous tile (that product completed before this
+            // tile's scores were signalled); scale it to the new max before P_t is released.
+            if (rescale && i > 0) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(trow + o_col + c * 32, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                    ptx::tmem_st32(trow + o_col + c * 32, o);
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(p_full + t);
+        }
+        // epilogue: O / l -> bf16
+        if (ok && ptx::mbar_wait(o_full + t, 0, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)) {
+            ptx::tc_fence_after();
+            const float inv = (owned && l > 0.f) ? 1.0f / l : 0.f;
+            uint16_t *dst = a.out + (static_cast<int64_t>(tok) * a.Hq + hq) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (n_iter > 0) {
+                    ptx::tmem_ld32(trow + o_col + c * 32, o);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = 0u;
+                }
+                if (row_ok) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        pk[j] = ptx::pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                }
+            }
+            if (row_ok && a.lse) {
+                const float v = (owned && l > 0.f) ? (((m == -INFINITY) ? 0.f : m) + __log2f(l)) * kLn2 : -INFINITY;
+                a.lse[static_cast<int64_t>(hq) * a.rows + tok] = v;
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+}  // namespace blink
+
+extern "C" size_t blink_attention_workspace(int32_t rows, int32_t B, int32_t P, int32_t Hq, int32_t Hkv, int32_t d)
+{
+    (void)rows;
+    (void)B;
+    (void)P;
+    (void)Hq;
+    (void)Hkv;
+    (void)d;
+    return blink::kHeaderBytes;
+}
+
+extern "C" blink_status blink_prefix_tail_attention(const blink_bf16 *q, const blink_bf16 *k_pre,
+                                                    const blink_bf16 *v_pre, int64_t pre_row_stride,
+                                                    const blink_bf16 *k_tail, const blink_bf16 *v_tail,
+                                                    const int32_t *d_cu_seqlens, const int32_t *d_seq_start,
+                                                    int32_t B, int32_t rows, int32_t P, int32_t max_tail, int32_t Hq,
+                                                    int32_t Hkv, int32_t d, float scale, blink_bf16 *out, float *lse,
+                                                    void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    using namespace blink;
+    if (!q || !k_tail || !v_tail || !d_cu_seqlens || !out || !d_ws) return BLINK_INVALID_ARG;
+    if (P < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 64 && d != 128) || rows < 1 || max_tail < 1)
+        return BLINK_INVALID_ARG;
+    const int g = Hq / Hkv;
+    if (g > BM) return BLINK_INVALID_ARG;
+    if (B < 1 || B > BLINK_MAX_PLAN_SEQUENCES) return BLINK_OUT_OF_RANGE;
+    if (static_cast<int64_t>(P) + max_tail > BLINK_MAX_INPUT_TOKENS) return BLINK_OUT_OF_RANGE;
+    if (P > 0) {
+        if (!k_pre || !v_pre) return BLINK_INVALID_ARG;
+        if (pre_row_stride < static_cast<int64_t>(Hkv) * d || pre_row_stride % 8 != 0) return BLINK_INVALID_ARG;
+        if (!aligned16(k_pre) || !aligned16(v_pre)) return BLINK_INVALID_ARG;
+    }
+    if (!aligned16(q) || !aligned16(k_tail) || !aligned16(v_tail) || !aligned16(out)) return BLINK_INVALID_ARG;
+    if (ws_bytes < blink_attention_workspace(rows, B, P, Hq, Hkv, d)) return BLINK_WORKSPACE_TOO_SMALL;
+
+    const int tpt = BM / g;
+    const int64_t tiles = (static_cast<int64_t>(rows) + tpt - 1) / tpt;
+    const int64_t pairs = (tiles + 1) / 2;
+    if (pairs > 0x7FFFFFFF || Hkv > 65535) return BLINK_OUT_OF_RANGE;
+
+    CUtensorMap tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail;
+    const uint64_t e = 2;  // bytes per bf16
+    bool ok = encode_tmap_3d_bf16(&tm_q, q, d, Hq, rows, d * e, static_cast<uint64_t>(Hq) * d * e, 64, g, tpt);
+    ok = ok && encode_tmap_3d_bf16(&tm_ktail, k_tail, d, Hkv, rows, d * e, static_cast<uint64_t>(Hkv) * d * e, 64,
+                                   1, BN);
+    ok = ok && encode_tmap_3d_bf16(&tm_vtail, v_tail, d, Hkv, rows, d * e, static_cast<uint64_t>(Hkv) * d * e, 64,
+                                   1, BN);
+    if (P > 0) {
+        ok = ok && encode_tmap_3d_bf16(&tm_kpre, k_pre, d, Hkv, P, d * e, static_cast<uint64_t>(pre_row_stride) * e,
+                                       64, 1, BN);
+        ok = ok && encode_tmap_3d_bf16(&tm_vpre, v_pre, d, Hkv, P, d * e, static_cast<uint64_t>(pre_row_stride) * e,
+                                       64, 1, BN);
+    } else {
+        tm_kpre = tm_ktail;  // never read: no prefix tiles
+        tm_vpre = tm_vtail;
+    }
+    if (!ok) return BLINK_CUDA_ERROR;
+
+    AttnArgs a;
+    a.cu = d_cu_seqlens;
+    a.seq_start = d_seq_start;
+    a.out = out;
+    a.lse = lse;
+    a.err = &static_cast<WorkspaceHeader *>(d_ws)->error;
+    a.rows = rows;
+    a.B = B;
+    a.P = P;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.g = g;
+    a.tpt = tpt;
+    a.n_pre = (P + BN - 1) / BN;
+    a.max_tail = max_tail;
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
+    a.scale_log2 = sc * kLog2e;
+
+    dim3 grid(static_cast<unsigned>(pairs), static_cast<unsigned>(Hkv));
+    if (d == 128) {
+        const int smem = Layout<128>::kAlloc;
+        if (cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        attention_kernel<128><<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
+    } else {
+        // Reserve enough shared memory that only one block fits per SM: each block takes all
+        // 512 tensor-memory columns.
+        const int smem = Layout<64>::kAlloc > 120 * 1024 ? Layout<64>::kAlloc : 120 * 1024;
+        if (cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        attention_kernel<64><<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
+    }
+    if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+    return BLINK_OK;
+}

@@ -1,0 +1,210 @@
+// readout.cu -- fused label readout (blink.py `_read` / `_read_batched` and `softmax`).
+//
+// Work unit: one (question, offered label) pair, i.e. one row of the CSR label list.  A warp
+// takes a row, streams that label's unembedding row with 16-byte loads (the HBM-bound part),
+// dots it with the question's last hidden state in FP32 and stages the logit in the output.
+// The warp that completes a question's last row (an atomic ticket per question, no spinning)
+// then applies the temperature softmax over that question's logits in place.  Consecutive rows
+// of a block belong to the same question, so the hidden state is reused from L1.
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace blink {
+namespace {
+
+constexpr int kReadoutWarps = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc)
+{
+    acc = fmaf(bf16_lo(a.x), bf16_lo(b.x), acc);
+    acc = fmaf(bf16_hi(a.x), bf16_hi(b.x), acc);
+    acc = fmaf(bf16_lo(a.y), bf16_lo(b.y), acc);
+    acc = fmaf(bf16_hi(a.y), bf16_hi(b.y), acc);
+    acc = fmaf(bf16_lo(a.z), bf16_lo(b.z), acc);
+    acc = fmaf(bf16_hi(a.z), bf16_hi(b.z), acc);
+    acc = fmaf(bf16_lo(a.w), bf16_lo(b.w), acc);
+    acc = fmaf(bf16_hi(a.w), bf16_hi(b.w), acc);
+    return acc;
+}
+
+// Largest b in [0, B) with off[b] <= r (off ascending); clamps to a valid index on bad input.
+__device__ __forceinline__ int question_of(const int32_t *__restrict__ off, int B, int r)
+{
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(off + mid) <= r)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kReadoutWarps * 32)
+    readout_kernel(const uint16_t *__restrict__ hidden, int64_t hstride, int hidden_rows,
+                   const int32_t *__restrict__ last_idx, const int32_t *__restrict__ slot_of,
+                   const uint16_t *__restrict__ unembed, int V, int H,
+                   const int32_t *__restrict__ label_off, const int32_t *__restrict__ label_ids, int B, int sum_k,
+                   float log2e_over_t, float *__restrict__ probs, float *__restrict__ logits,
+                   uint32_t *__restrict__ counters, int *__restrict__ err)
+{
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Distributed check of the CSR offsets: block c checks questions c, c + grid, ...
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b <= B; b += gridDim.x * blockDim.x) {
+        bool ok = true;
+        if (b == 0) ok = __ldg(label_off) == 0;
+        if (b == B) ok = ok && __ldg(label_off + B) == sum_k;
+        if (b < B) {
+            int k = __ldg(label_off + b + 1) - __ldg(label_off + b);
+            ok = ok && k >= 1 && k <= BLINK_MAX_OPTIONS;
+        }
+        if (!ok) atomicCAS(err, 0, BLINK_DEVICE_FLAG);
+    }
+
+    const int r = blockIdx.x * kReadoutWarps + warp;
+    if (r >= sum_k) return;
+    const int b = question_of(label_off, B, r);
+    const int lo = max(0, min(sum_k, __ldg(label_off + b)));
+    const int hi = max(lo, min(sum_k, __ldg(label_off + b + 1)));
+    const int K = hi - lo;
+    if (r < lo || r >= hi) {  // malformed offsets: the row is not inside its question
+        if (lane == 0) atomicCAS(err, 0, BLINK_DEVICE_FLAG);
+        return;
+    }
+    const int id = __ldg(label_ids + r);
+    int li = b;
+    if (slot_of) {
+        li = __ldg(slot_of + b);
+        if (li < 0 || li >= B) li = -1;
+    }
+    const int hrow = li < 0 ? -1 : __ldg(last_idx + li);
+    const bool bad = id < 0 || id >= V || hrow < 0 || hrow >= hidden_rows;
+
+    float acc = 0.f;
+    if (!bad) {
+        const uint4 *w = reinterpret_cast<const uint4 *>(unembed + static_cast<int64_t>(id) * H);
+        const uint4 *h = reinterpret_cast<const uint4 *>(hidden + static_cast<int64_t>(hrow) * hstride);
+        const int nchunk = H >> 3;  // 8 bf16 per 16-byte chunk
+        int c = lane;
+        for (; c + 96 < nchunk; c += 128) {
+            uint4 w0 = ld_stream(w + c), w1 = ld_stream(w + c + 32), w2 = ld_stream(w + c + 64),
+                  w3 = ld_stream(w + c + 96);
+            uint4 h0 = __ldg(h + c), h1 = __ldg(h + c + 32), h2 = __ldg(h + c + 64), h3 = __ldg(h + c + 96);
+            acc = dot8(w0, h0, acc);
+            acc = dot8(w1, h1, acc);
+            acc = dot8(w2, h2, acc);
+            acc = dot8(w3, h3, acc);
+        }
+        for (; c < nchunk; c += 32) acc = dot8(ld_stream(w + c), __ldg(h + c), acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+
+    uint32_t ticket = 0;
+    if (lane == 0) {
+        const float z = bad ? __int_as_float(0x7FC00000) : acc;
+        probs[r] = z;  // staged here until the question's softmax
+        if (logits) logits[r] = z;
+        if (bad) atomicCAS(err, 0, BLINK_DEVICE_FLAG);
+        __threadfence();
+        ticket = atomicInc(counters + b, static_cast<uint32_t>(K - 1));  // wraps back to 0 on the last
+    }
+    ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
+    if (ticket != static_cast<uint32_t>(K - 1)) return;
+
+    // This warp completed question b: temperature softmax over its K staged logits.
+    __threadfence();
+    float v[8];
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int k = lo + lane + 32 * j;
+        v[j] = k < hi ? __ldcg(probs + k) * log2e_over_t : -INFINITY;
+        m = fmaxf(m, v[j]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int k = lo + lane + 32 * j;
+        v[j] = k < hi ? exp2f(v[j] - m) : 0.f;
+        s += v[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    const float inv = 1.0f / s;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int k = lo + lane + 32 * j;
+        if (k < hi) probs[k] = v[j] * inv;
+    }
+}
+
+}  // namespace
+}  // namespace blink
+
+extern "C" size_t blink_label_readout_workspace(int32_t B)
+{
+    if (B < 1) return 0;
+    return blink::kHeaderBytes + blink::align_up(static_cast<size_t>(B) * sizeof(uint32_t), 256);
+}
+
+extern "C" blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hidden_row_stride, int32_t hidden_rows,
+                                            const int32_t *d_last_idx, const int32_t *d_slot_of,
+                                            const blink_bf16 *unembed, int32_t V, int32_t H,
+                                            const int32_t *d_label_off, const int32_t *d_label_ids, int32_t B,
+                                            int32_t sum_k, float temperature, float *d_probs, float *h_probs,
+                                            float *d_logits, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    using namespace blink;
+    if (!hidden || !d_last_idx || !unembed || !d_label_off || !d_label_ids || !d_probs || !d_ws)
+        return BLINK_INVALID_ARG;
+    if (!(temperature > 0.f) || !(temperature < INFINITY)) return BLINK_INVALID_ARG;  // blink.py `decide`
+    if (V < 1 || H < 8 || H % 8 != 0 || hidden_rows < 1 || hidden_row_stride < H || hidden_row_stride % 8 != 0)
+        return BLINK_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(unembed)) return BLINK_INVALID_ARG;
+    if (B < 1 || B > BLINK_MAX_PLAN_SEQUENCES) return BLINK_OUT_OF_RANGE;
+    if (sum_k < B || static_cast<int64_t>(sum_k) > static_cast<int64_t>(B) * BLINK_MAX_OPTIONS)
+        return BLINK_OUT_OF_RANGE;
+    if (ws_bytes < blink_label_readout_workspace(B)) return BLINK_WORKSPACE_TOO_SMALL;
+
+    auto *hdr = static_cast<WorkspaceHeader *>(d_ws);
+    auto *counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(d_ws) + kHeaderBytes);
+    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(B) * sizeof(uint32_t), stream) != cudaSuccess)
+        return BLINK_CUDA_ERROR;
+    const int grid = (sum_k + kReadoutWarps - 1) / kReadoutWarps;
+    const float log2e_over_t = kLog2e / temperature;
+    readout_kernel<<<grid, kReadoutWarps * 32, 0, stream>>>(hidden, hidden_row_stride, hidden_rows, d_last_idx,
+                                                           d_slot_of, unembed, V, H, d_label_off, d_label_ids, B, sum_k,
+                                                           log2e_over_t, d_probs, d_logits, counters, &hdr->error);
+    if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+    if (h_probs) {
+        int32_t word = 0;
+        if (cudaMemcpyAsync(h_probs, d_probs, static_cast<size_t>(sum_k) * sizeof(float), cudaMemcpyDeviceToHost,
+                            stream) != cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        if (cudaMemcpyAsync(&word, &hdr->error, sizeof word, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return BLINK_CUDA_ERROR;
+        if (word != 0) return word == BLINK_DEVICE_TIMEOUT ? BLINK_DEVICE_TIMEOUT : BLINK_DEVICE_FLAG;
+    }
+    return BLINK_OK;
+}

@@ -1,0 +1,117 @@
+"""tcgen05 prefix-tail attention vs the FP64 oracle (blink.py PREFIX_CACHE note, `_forward_shared`).
+
+Small cases are compared on every output row; the full-size workloads on sampled (token, head)
+pairs that include every question's first and last tail row.  Tolerance: max |O - O_ref| within
+2e-2 of max |O_ref|; LSE within 2e-3 (absolute, natural log, scaled for large values).
+"""
+import numpy as np
+import pytest
+import torch
+
+from shared_prefix_question_gb300 import blink
+from shared_prefix_question_gb300 import workloads as wl
+from tests.helpers import compare_attention, dev_bf16, run_attention, sample_pairs
+
+pytestmark = pytest.mark.gpu
+
+
+def _w(name, index, P, Hq, Hkv, d):
+    return wl.Workload(name, index, P, 0, 1, 1, Hq, Hkv, d, 8, 8, 1, 1, 1.0, "letters")
+
+
+SMALL = [
+    # name, P, lengths, Hq, Hkv, d
+    ("tiny", 64, [8, 12, 16, 24], 4, 2, 64),
+    ("ragged-prefix-g4", 200, [1, 5, 37, 130, 3], 8, 2, 128),
+    ("g5", 300, [10, 70, 25], 10, 2, 128),
+    ("g1-d64", 129, [3, 200], 2, 2, 64),
+    ("no-prefix", 0, [1, 17, 300, 64], 8, 2, 128),
+    ("g8", 256, [33, 7], 16, 2, 128),
+    ("many-short", 77, list(np.random.default_rng(3).integers(1, 5, size=40)), 8, 2, 128),
+    ("single-row", 1, [1], 4, 4, 64),
+    ("long-tail", 128, [700, 2], 4, 1, 128),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: c[0])
+def test_attention_small_all_rows(case):
+    name, P, lengths, Hq, Hkv, d = case
+    ins = wl.attention_inputs(_w(name, 300 + len(name), P, Hq, Hkv, d), lengths=np.array(lengths), P=P)
+    out, lse, st = run_attention(ins)
+    assert st == blink.BLINK_OK
+    compare_attention(ins, out, lse)
+
+
+def test_attention_padded_layout():
+    P, lengths, width = 130, [5, 40, 1], 48
+    ins = wl.attention_inputs(_w("pad", 400, P, 4, 1, 128), lengths=np.array(lengths), P=P, padded_width=width)
+    out, lse, st = run_attention(ins, padded=True)
+    assert st == blink.BLINK_OK
+    compare_attention(ins, out, lse)
+    owned = np.zeros(ins.rows, dtype=bool)
+    for s, L in zip(ins.seq_start, ins.seq_len):
+        owned[s:s + L] = True
+    assert (out[~owned] == 0).all()
+    assert np.isneginf(lse[:, ~owned]).all()
+
+
+def test_attention_arena_slice():
+    """The prefix is a region of a wider KV arena (simit engine.py: one arena, a region per
+    request): rows start at an arena offset and are `stride` elements apart."""
+    P, Hq, Hkv, d = 300, 8, 2, 128
+    ins = wl.attention_inputs(_w("arena", 401, P, Hq, Hkv, d), lengths=np.array([20, 9]), P=P)
+    stride = Hkv * d + 64
+    kstart = 37
+    arena_k = torch.zeros(kstart + P + 5, stride, dtype=torch.bfloat16, device="cuda")
+    arena_v = torch.zeros_like(arena_k)
+    arena_k[kstart:kstart + P, :Hkv * d] = dev_bf16(ins.k_pre).reshape(P, -1)
+    arena_v[kstart:kstart + P, :Hkv * d] = dev_bf16(ins.v_pre).reshape(P, -1)
+    out, lse, st = run_attention(ins, pre_row_stride=stride, k_pre_dev=arena_k[kstart], v_pre_dev=arena_v[kstart])
+    assert st == blink.BLINK_OK
+    compare_attention(ins, out, lse)
+
+
+def test_attention_cu_slice_offsets():
+    """A slice of a larger cu_seqlens array (cu[0] != 0) with pointers offset by cu[0] rows."""
+    from tests.helpers import dev_i32, host_f64
+    P, Hq, Hkv, d = 150, 4, 2, 64
+    lengths = np.array([6, 9, 4, 11])
+    ins = wl.attention_inputs(_w("slice", 402, P, Hq, Hkv, d), lengths=lengths, P=P)
+    q, kt, vt = dev_bf16(ins.q), dev_bf16(ins.k_tail), dev_bf16(ins.v_tail)
+    kp, vp = dev_bf16(ins.k_pre), dev_bf16(ins.v_pre)
+    cu = dev_i32(ins.cu_seqlens)
+    base = int(ins.cu_seqlens[2])
+    out, lse, ws = blink.blink_prefix_tail_attention(q[base:], kp, vp, kt[base:], vt[base:], cu[2:], B=2, P=P,
+                                                     max_tail=11, want_lse=True)
+    torch.cuda.synchronize()
+    assert blink.blink_read_device_status(ws) == blink.BLINK_OK
+    full = np.full((ins.rows, Hq, d), np.nan)
+    full[base:] = host_f64(out)
+    full_lse = np.full((Hq, ins.rows), np.nan)
+    full_lse[:, base:] = host_f64(lse)
+    toks = np.arange(base, ins.rows, dtype=np.int32)
+    for h in range(Hq):
+        compare_attention(ins, full, full_lse, select=(toks, np.full_like(toks, h)))
+
+
+def test_attention_device_flag_on_bad_length():
+    """A question longer than max_tail is flagged on the device (no trap); other rows still run."""
+    P = 64
+    ins = wl.attention_inputs(_w("flag", 403, P, 4, 2, 64), lengths=np.array([8, 30]), P=P)
+    out, lse, st = run_attention(ins, max_tail=16)
+    assert st == blink.BLINK_DEVICE_FLAG
+
+
+@pytest.mark.parametrize("name,n_sample", [("2k", 0), ("18k", 768), ("plain", 768), ("max", 256)])
+def test_attention_workloads(name, n_sample):
+    w = wl.WORKLOADS[name]
+    ins = wl.attention_inputs(w)
+    out, lse, st = run_attention(ins)
+    assert st == blink.BLINK_OK
+    if n_sample == 0:
+        compare_attention(ins, out, lse)
+    else:
+        compare_attention(ins, out, lse, select=sample_pairs(ins, n_sample, seed=w.index))
+    # every owned row finite (the sampled check covers values; this covers the rest)
+    rows = np.concatenate([np.arange(s, s + L) for s, L in zip(ins.seq_start, ins.seq_len)])
+    assert np.isfinite(out[rows]).all()

@@ -1,0 +1,101 @@
+"""Fused label readout vs the FP64 oracle (blink.py `_read` / `_read_batched`, `softmax`).
+
+Probabilities within 1e-3 absolute and the same argmax (ties to the first label in request
+order, as blink.py's answer assembly breaks them); a near-tie (oracle logit gap < 1e-4)
+accepts either of the two.
+"""
+import numpy as np
+import pytest
+import torch
+
+from shared_prefix_question_gb300 import blink
+from shared_prefix_question_gb300 import workloads as wl
+from tests.helpers import compare_readout, dev_bf16, dev_i32
+
+pytestmark = pytest.mark.gpu
+
+_UNEMBED = {}
+
+
+def _unembed(w):
+    key = (w.V, w.H)
+    if key not in _UNEMBED:
+        rng = np.random.default_rng(7000 + w.H)
+        _UNEMBED.clear()
+        _UNEMBED[key] = wl.normal_bf16(rng, (w.V, w.H), std=0.02)
+    return _UNEMBED[key]
+
+
+def _run(ins, host=True, logits=False):
+    hidden = dev_bf16(ins.hidden)
+    W = dev_bf16(ins.unembed)
+    sum_k = len(ins.label_ids)
+    hp = torch.empty(sum_k, dtype=torch.float32, pin_memory=True) if host else None
+    lg = torch.empty(sum_k, dtype=torch.float32, device="cuda") if logits else None
+    probs, ws = blink.blink_label_readout(hidden, dev_i32(ins.last_idx), W, dev_i32(ins.label_off),
+                                          dev_i32(ins.label_ids), ins.temperature, host_probs=hp, logits=lg)
+    torch.cuda.synchronize()
+    out = hp.numpy().astype(np.float64) if host else probs.cpu().numpy().astype(np.float64)
+    return out, (lg.cpu().numpy() if logits else None), ws
+
+
+@pytest.mark.parametrize("name", ["tiny", "2k", "18k", "plain", "max", "readout_stress"])
+def test_readout_workloads(name):
+    w = wl.WORKLOADS[name]
+    ins = wl.readout_inputs(w, unembed=None if name == "tiny" else _unembed(w))
+    probs, _, _ = _run(ins)
+    compare_readout(probs, ins)
+
+
+def test_readout_device_copy_and_logits():
+    w = wl.WORKLOADS["tiny"]
+    ins = wl.readout_inputs(w)
+    probs, logits, _ = _run(ins, host=False, logits=True)
+    compare_readout(probs, ins)
+    from oracle import oracle
+    z, _, _ = oracle.label_readout(ins.hidden, ins.last_idx, ins.unembed, ins.label_off, ins.label_ids, 1.0)
+    assert np.abs(logits - z).max() < 1e-4
+
+
+def test_readout_special_cases():
+    rng = np.random.default_rng(11)
+    H, V = 264, 500
+    hidden = wl.normal_bf16(rng, (5, H))
+    W = wl.normal_bf16(rng, (V, H), std=0.05)
+    # one label -> 1; a repeated id -> uniform; 255 labels (the maximum)
+    off = np.array([0, 1, 5, 5 + 255], dtype=np.int32)
+    ids = np.concatenate([[3], [7, 7, 7, 7], rng.choice(V, 255, replace=False)]).astype(np.int32)
+    ins = wl.ReadoutInputs(hidden, np.array([4, 0, 2], dtype=np.int32), W, off, ids, 0.37)
+    probs, _, _ = _run(ins)
+    assert probs[0] == 1.0
+    np.testing.assert_allclose(probs[1:5], 0.25, atol=1e-7)
+    compare_readout(probs, ins)
+
+
+def test_readout_bad_label_flagged():
+    rng = np.random.default_rng(12)
+    H, V = 64, 100
+    hidden = wl.normal_bf16(rng, (2, H))
+    W = wl.normal_bf16(rng, (V, H))
+    off = np.array([0, 2, 4], dtype=np.int32)
+    ids = np.array([1, 2, 3, V], dtype=np.int32)  # the last id is out of range
+    hp = torch.empty(4, dtype=torch.float32, pin_memory=True)
+    with pytest.raises(blink.BlinkError) as e:
+        blink.blink_label_readout(dev_bf16(hidden), dev_i32([0, 1]), dev_bf16(W), dev_i32(off), dev_i32(ids), 1.0,
+                                  host_probs=hp)
+    assert e.value.status == blink.BLINK_DEVICE_FLAG
+    p = hp.numpy()
+    assert np.isfinite(p[:2]).all() and abs(p[:2].sum() - 1) < 1e-6
+    assert np.isnan(p[2:]).all()
+
+
+def test_readout_repeated_calls_reuse_workspace():
+    w = wl.WORKLOADS["tiny"]
+    ins = wl.readout_inputs(w)
+    hidden, W = dev_bf16(ins.hidden), dev_bf16(ins.unembed)
+    last, off, ids = dev_i32(ins.last_idx), dev_i32(ins.label_off), dev_i32(ins.label_ids)
+    ws = None
+    for _ in range(3):
+        probs, ws = blink.blink_label_readout(hidden, last, W, off, ids, 1.0, ws=ws)
+        torch.cuda.synchronize()
+        compare_readout(probs.cpu().numpy().astype(np.float64), ins)
