@@ -121,7 +121,9 @@ blink_status blink_pack_plan(const int32_t *d_lengths, int32_t n, int32_t budget
  * B                      1..BLINK_MAX_PLAN_SEQUENCES questions
  * rows                   token rows of q / k_tail / v_tail / out (>= 1)
  * P                      prefix length, 0 (plain causal path) .. 131072
- * max_tail               upper bound of len_b, checked on the device; P + max_tail <= 131072
+ * max_tail               upper bound of len_b, checked on the device; P and max_tail are each at
+ *                        most 131072 (blink.py MAX_INPUT_TOKENS bounds one rendered prompt; the
+ *                        largest request keeps a full 131072-token prefix plus its tails)
  * Hq, Hkv, d             Hq % Hkv == 0, Hq/Hkv <= 128, d in {64, 128}
  * scale                  softmax scale; <= 0 selects 1/sqrt(d)
  * out   [rows, Hq, d]    bf16 (round to nearest even)

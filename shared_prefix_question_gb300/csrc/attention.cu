@@ -471,7 +471,7 @@ extern "C" blink_status blink_prefix_tail_attention(const blink_bf16 *q, const b
     const int g = Hq / Hkv;
     if (g > BM) return BLINK_INVALID_ARG;
     if (B < 1 || B > BLINK_MAX_PLAN_SEQUENCES) return BLINK_OUT_OF_RANGE;
-    if (static_cast<int64_t>(P) + max_tail > BLINK_MAX_INPUT_TOKENS) return BLINK_OUT_OF_RANGE;
+    if (P > BLINK_MAX_INPUT_TOKENS || max_tail > BLINK_MAX_INPUT_TOKENS) return BLINK_OUT_OF_RANGE;
     if (P > 0) {
         if (!k_pre || !v_pre) return BLINK_INVALID_ARG;
         if (pre_row_stride < static_cast<int64_t>(Hkv) * d || pre_row_stride % 8 != 0) return BLINK_INVALID_ARG;

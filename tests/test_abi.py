@@ -81,7 +81,8 @@ def test_attention_host_checks(lib):
                                              Hkv, d, 0.0, FAKE, None, FAKE, ws, None)
     assert call(d=96) == blink.BLINK_INVALID_ARG
     assert call(Hq=6, Hkv=4) == blink.BLINK_INVALID_ARG
-    assert call(P=131072, max_tail=1) == blink.BLINK_OUT_OF_RANGE   # past MAX_INPUT_TOKENS
+    assert call(P=131073, max_tail=1) == blink.BLINK_OUT_OF_RANGE   # past MAX_INPUT_TOKENS
+    assert call(max_tail=131073) == blink.BLINK_OUT_OF_RANGE
     assert call(B=0) == blink.BLINK_OUT_OF_RANGE
     assert call(stride=100) == blink.BLINK_INVALID_ARG               # stride below Hkv * d
     assert call(kpre=None) == blink.BLINK_INVALID_ARG                # prefix pointers missing
