@@ -176,6 +176,36 @@ blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hidden_row_st
                                  int32_t sum_k, float temperature, float *d_probs, float *h_probs,
                                  float *d_logits, void *d_ws, size_t ws_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Label readout that allocates nothing.  The pages have no counterpart: this entry point is an
+ * addition of this library for callers that cannot hand it a workspace.
+ *
+ * Who needs it: code embedded in a host that gives it only its input and output buffers and
+ * owns every other byte of device memory (a serving runtime with a fixed memory plan made at
+ * start-up), and latency-critical loops that must never call cudaMalloc, which may synchronise
+ * the whole device.  Such callers cannot provide the `d_ws` that blink_label_readout needs.
+ *
+ * Arguments and results are those of blink_label_readout without d_ws / ws_bytes.  The scratch
+ * (an error word and one ticket per question) is a static device array of
+ * 256 + 4 * BLINK_STATIC_SCRATCH_QUESTIONS bytes (128.25 KiB) that every GPU which loads this
+ * library keeps until the process exits.
+ *   - B above BLINK_STATIC_SCRATCH_QUESTIONS returns BLINK_OUT_OF_RANGE; nothing is launched.
+ *   - The first call on a device looks up the array's device address with that device current
+ *     (cudaGetSymbolAddress); make that first call before any stream capture on the device.
+ *   - Every call first clears the array's error word and tickets on `stream`.  All calls share
+ *     the one array, which keeps the last call's contents: calls whose work can overlap on the
+ *     GPU (different streams with no ordering between them) race, and must not be made.
+ *   - Device-side errors are reported only through the host-output path (h_probs != NULL).
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ * ------------------------------------------------------------------------------------------ */
+#define BLINK_STATIC_SCRATCH_QUESTIONS 32768
+
+blink_status blink_label_readout_noalloc(const blink_bf16 *hidden, int64_t hidden_row_stride, int32_t hidden_rows,
+                                         const int32_t *d_last_idx, const int32_t *d_slot_of,
+                                         const blink_bf16 *unembed, int32_t V, int32_t H, const int32_t *d_label_off,
+                                         const int32_t *d_label_ids, int32_t B, int32_t sum_k, float temperature,
+                                         float *d_probs, float *h_probs, float *d_logits, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -53,6 +53,8 @@ _SIGNATURES = {
     "blink_label_readout_workspace": (_sz, [_i32]),
     "blink_label_readout": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
                                    _vp, _sz, _vp]),
+    "blink_label_readout_noalloc": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _f32, _vp,
+                                           _vp, _vp, _vp]),
 }
 
 
@@ -195,3 +197,26 @@ def blink_label_readout(hidden, last_idx, unembed, label_off, label_ids, tempera
                                    ws.numel(), _stream(stream))
     _check(st, "blink_label_readout")
     return probs, ws
+
+
+STATIC_SCRATCH_QUESTIONS = 32768
+
+
+def blink_label_readout_noalloc(hidden, last_idx, unembed, label_off, label_ids, temperature: float, probs=None,
+                                host_probs=None, logits=None, slot_of=None, stream=None):
+    """The readout for callers that cannot allocate device memory (the library keeps its scratch in a
+    static device array; at most 32768 questions; calls that overlap on the GPU race).  Outputs are
+    allocated here only when the caller passes none."""
+    _need_cuda(hidden, last_idx, unembed, label_off, label_ids, probs, logits, slot_of)
+    rows, H = hidden.shape
+    V = unembed.shape[0]
+    B = label_off.numel() - 1
+    sum_k = label_ids.numel()
+    if probs is None:
+        probs = torch.empty(sum_k, dtype=torch.float32, device=hidden.device)
+    st = lib().blink_label_readout_noalloc(_ptr(hidden), int(hidden.stride(0)), int(rows), _ptr(last_idx),
+                                           _ptr(slot_of), _ptr(unembed), int(V), int(H), _ptr(label_off),
+                                           _ptr(label_ids), int(B), int(sum_k), float(temperature), _ptr(probs),
+                                           _ptr(host_probs), _ptr(logits), _stream(stream))
+    _check(st, "blink_label_readout_noalloc")
+    return probs

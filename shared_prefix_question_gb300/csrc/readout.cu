@@ -7,6 +7,7 @@
 // then applies the temperature softmax over that question's logits in place.  Consecutive rows
 // of a block belong to the same question, so the hidden state is reused from L1.
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -202,6 +203,83 @@ extern "C" blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hi
                             stream) != cudaSuccess)
             return BLINK_CUDA_ERROR;
         if (cudaMemcpyAsync(&word, &hdr->error, sizeof word, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return BLINK_CUDA_ERROR;
+        if (word != 0) return word == BLINK_DEVICE_TIMEOUT ? BLINK_DEVICE_TIMEOUT : BLINK_DEVICE_FLAG;
+    }
+    return BLINK_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// The same readout for callers that cannot allocate device memory: the scratch (error word and
+// one ticket per question) lives in a static device array owned by this file.
+// ---------------------------------------------------------------------------------------------
+namespace blink {
+namespace {
+
+constexpr int kStaticMaxDevices = 64;
+constexpr int kStaticHeaderWords = 64;  // 256 bytes: the error word, then reserved
+// Held by every GPU that loads the library, until the process exits.
+static __device__ __align__(256) uint32_t g_readout_scratch[kStaticHeaderWords + BLINK_STATIC_SCRATCH_QUESTIONS];
+
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kStaticMaxDevices] = {};
+
+// Device address of g_readout_scratch on the current device, looked up once per device (the
+// array's name is only a host-side stand-in in host code).
+void *scratch_address()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_readout_scratch) != cudaSuccess) return nullptr;
+        g_scratch_addr[dev] = p;
+    }
+    return g_scratch_addr[dev];
+}
+
+}  // namespace
+}  // namespace blink
+
+extern "C" blink_status blink_label_readout_noalloc(const blink_bf16 *hidden, int64_t hidden_row_stride,
+                                                    int32_t hidden_rows, const int32_t *d_last_idx,
+                                                    const int32_t *d_slot_of, const blink_bf16 *unembed, int32_t V,
+                                                    int32_t H, const int32_t *d_label_off, const int32_t *d_label_ids,
+                                                    int32_t B, int32_t sum_k, float temperature, float *d_probs,
+                                                    float *h_probs, float *d_logits, cudaStream_t stream)
+{
+    using namespace blink;
+    if (!hidden || !d_last_idx || !unembed || !d_label_off || !d_label_ids || !d_probs) return BLINK_INVALID_ARG;
+    if (!(temperature > 0.f) || !(temperature < INFINITY)) return BLINK_INVALID_ARG;
+    if (V < 1 || H < 8 || H % 8 != 0 || hidden_rows < 1 || hidden_row_stride < H || hidden_row_stride % 8 != 0)
+        return BLINK_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(unembed)) return BLINK_INVALID_ARG;
+    if (B < 1 || B > BLINK_STATIC_SCRATCH_QUESTIONS) return BLINK_OUT_OF_RANGE;
+    if (sum_k < B || static_cast<int64_t>(sum_k) > static_cast<int64_t>(B) * BLINK_MAX_OPTIONS)
+        return BLINK_OUT_OF_RANGE;
+
+    void *scratch = scratch_address();
+    if (!scratch) return BLINK_CUDA_ERROR;
+    auto *err = static_cast<int *>(scratch);
+    auto *counters = static_cast<uint32_t *>(scratch) + kStaticHeaderWords;
+    // Calls share the array: clear this call's error word and tickets first.
+    if (cudaMemsetAsync(scratch, 0, (kStaticHeaderWords + static_cast<size_t>(B)) * sizeof(uint32_t), stream) !=
+        cudaSuccess)
+        return BLINK_CUDA_ERROR;
+    const int grid = (sum_k + kReadoutWarps - 1) / kReadoutWarps;
+    readout_kernel<<<grid, kReadoutWarps * 32, 0, stream>>>(hidden, hidden_row_stride, hidden_rows, d_last_idx,
+                                                           d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
+                                                           sum_k, kLog2e / temperature, d_probs, d_logits, counters,
+                                                           err);
+    if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+    if (h_probs) {
+        int32_t word = 0;
+        if (cudaMemcpyAsync(h_probs, d_probs, static_cast<size_t>(sum_k) * sizeof(float), cudaMemcpyDeviceToHost,
+                            stream) != cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        if (cudaMemcpyAsync(&word, err, sizeof word, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
             return BLINK_CUDA_ERROR;
         if (cudaStreamSynchronize(stream) != cudaSuccess) return BLINK_CUDA_ERROR;
         if (word != 0) return word == BLINK_DEVICE_TIMEOUT ? BLINK_DEVICE_TIMEOUT : BLINK_DEVICE_FLAG;
