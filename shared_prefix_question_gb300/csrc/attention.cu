@@ -235,19 +235,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t o_col[2] = {256u, 256u + D};
             const uint32_t q_addr[2] = {ptx::smem_u32(q_s0), ptx::smem_u32(q_s1)};
             const uint32_t kv_addr = ptx::smem_u32(kv_s);
-            auto qk = [&](int t, uint32_t k_addr) {
+            // Every shared-memory descriptor the loop needs, built once: Q tiles, the two K slots
+            // and the two V slots, per 16-wide k-step.
+            uint64_t qd[2][D / 16], kd[2][D / 16], vd[2][BN / 16];
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    ptx::mma_ss(tmem + s_col[t], ptx::smem_desc_sw128(q_addr[t] + off, 16, 1024),
-                                ptx::smem_desc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-                }
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                qd[0][kk] = ptx::smem_desc_sw128(q_addr[0] + off, 16, 1024);
+                qd[1][kk] = ptx::smem_desc_sw128(q_addr[1] + off, 16, 1024);
+                kd[0][kk] = ptx::smem_desc_sw128(kv_addr + 0 * L::kKVTileBytes + off, 16, 1024);
+                kd[1][kk] = ptx::smem_desc_sw128(kv_addr + 2 * L::kKVTileBytes + off, 16, 1024);
+            }
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+                vd[0][kk] = ptx::smem_desc_sw128(kv_addr + 1 * L::kKVTileBytes + kk * 2048, kHalfBytes, 1024);
+                vd[1][kk] = ptx::smem_desc_sw128(kv_addr + 3 * L::kKVTileBytes + kk * 2048, kHalfBytes, 1024);
+            }
+            auto qk = [&](int t, uint32_t k_addr) {
+                const bool hi = k_addr != kv_addr;  // K lives in slot 0 or slot 2
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + s_col[t], qd[t][kk], hi ? kd[1][kk] : kd[0][kk], idesc_s, kk > 0 ? 1u : 0u);
             };
             auto pv = [&](int t, uint32_t v_addr, bool first) {
+                const bool hi = v_addr != kv_addr + L::kKVTileBytes;  // V lives in slot 1 or slot 3
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    ptx::mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8,
-                                ptx::smem_desc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                    ptx::mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8, hi ? vd[1][kk] : vd[0][kk], idesc_pv,
                                 (!first || kk > 0) ? 1u : 0u);
             };
             bool ok = ptx::mbar_wait(q_full, 0, abort_flag, a.err, BLINK_DEVICE_TIMEOUT);
