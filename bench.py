@@ -29,7 +29,14 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "questions/sec and prefill tokens/sec at 1 GB300; % BF16 TC peak and % HBM BW"
-FLUSH_BYTES = 512 << 20  # written between timed steps: larger than the 129 MB L2
+FLUSH_BYTES = 512 << 20  # flushed between timed steps: larger than the 129 MB L2
+
+
+def flush_l2(buf):
+    """Evicts L2 between timed steps: write a buffer larger than L2, then read it back, so the
+    write-back of the dirty flush lines happens here and not inside the next timed region."""
+    buf.zero_()
+    buf.view(-1, 4096).amax(dim=1)
 
 
 def parse():
@@ -43,6 +50,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle sample")
+    ap.add_argument("--only", choices=["readout_stress"], default=None,
+                    help="run one sub-measurement alone (for profiling) and print its JSON")
     return ap.parse_args()
 
 
@@ -229,6 +238,10 @@ def main():
     from shared_prefix_question_gb300 import blink, build
     build.build()
     hbm_peak, tc_peak, tc_sustained, peak_kind = peaks()
+    if args.only == "readout_stress":
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        print(json.dumps(readout_stress(blink, dev, hbm_peak, peak_kind, flush, args)), flush=True)
+        return
 
     w, lengths, ins, rd = build_workload(args.workload)
 
@@ -273,7 +286,7 @@ def main():
             ev[3].record(stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2(flush)
         step()
     torch.cuda.synchronize()
     st = blink.blink_read_device_status(ws_a)
@@ -291,7 +304,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2(flush)
         step(evs[k])
     torch.cuda.synchronize()
     if world > 1:
@@ -327,7 +340,7 @@ def main():
             "config": {"workload": f"{w.name}: {w.description}", "P": ins.P, "questions": n,
                        "tail_tokens": int(lengths.sum()), "Hq": ins.Hq, "Hkv": ins.Hkv, "d": ins.d, "H": w.H,
                        "V": w.V, "labels": sum_k, "temperature": w.temperature, "budget": 32768,
-                       "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB write)",
+                       "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB written then read back)",
                        "parallelism": f"replicas x{world}, questions sharded, no collective in the step"},
             "prefill_tokens_per_s": world * prefill_tokens / (ms_per_step / 1000.0),
             "kernels_ms": {"plan": statistics.mean(plan_ms), "attention": attn_mean,
@@ -369,7 +382,7 @@ def readout_stress(blink, dev, hbm_peak, peak_kind, flush, args):
         blink.blink_label_readout(hidden, last, W, d_off, d_ids, 1.0, probs=probs, ws=ws)
     times = []
     for _ in range(max(10, args.steps)):
-        flush.zero_()
+        flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         blink.blink_label_readout(hidden, last, W, d_off, d_ids, 1.0, probs=probs, ws=ws)
@@ -434,7 +447,7 @@ def e2e(blink, dev, w, lengths, ins, rd, flush, args, world):
     if world > 1:
         dist.barrier()
     for _ in range(steps):
-        flush.zero_()
+        flush_l2(flush)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         one()  # ends with the readout's synchronising host copy

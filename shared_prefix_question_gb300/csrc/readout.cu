@@ -104,14 +104,15 @@ __global__ void __launch_bounds__(kReadoutWarps * 32)
         const uint4 *h = reinterpret_cast<const uint4 *>(hidden + static_cast<int64_t>(hrow) * hstride);
         const int nchunk = H >> 3;  // 8 bf16 per 16-byte chunk
         int c = lane;
-        for (; c + 96 < nchunk; c += 128) {
-            uint4 w0 = ld_stream(w + c), w1 = ld_stream(w + c + 32), w2 = ld_stream(w + c + 64),
-                  w3 = ld_stream(w + c + 96);
-            uint4 h0 = __ldg(h + c), h1 = __ldg(h + c + 32), h2 = __ldg(h + c + 64), h3 = __ldg(h + c + 96);
-            acc = dot8(w0, h0, acc);
-            acc = dot8(w1, h1, acc);
-            acc = dot8(w2, h2, acc);
-            acc = dot8(w3, h3, acc);
+        // eight 16-byte loads of the label row (and of the hidden row) in flight per lane
+        for (; c + 224 < nchunk; c += 256) {
+            uint4 wv[8], hv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) wv[u] = ld_stream(w + c + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) hv[u] = __ldg(h + c + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc = dot8(wv[u], hv[u], acc);
         }
         for (; c < nchunk; c += 32) acc = dot8(ld_stream(w + c), __ldg(h + c), acc);
     }
