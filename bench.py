@@ -142,6 +142,11 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def wl_question_types(w, label_off):
+    from shared_prefix_question_gb300 import workloads as wl
+    return wl.question_types(w, label_off)
+
+
 def build_workload(name: str):
     from shared_prefix_question_gb300 import workloads as wl
     w = wl.WORKLOADS[name]
@@ -257,7 +262,9 @@ def main():
     kp, vp = (bf(ins.k_pre), bf(ins.v_pre)) if ins.P else (None, None)
     hidden, W = bf(rd.hidden), bf(rd.unembed)
     off, ids = i32(rd.label_off), i32(rd.label_ids)
+    qtype = i32(wl_question_types(w, rd.label_off))
     n, sum_k = w.n, len(rd.label_ids)
+    answers = torch.empty(n, 3, dtype=torch.float32, device=dev)
     max_tail = int(lengths.max())
     plan = {k: torch.empty(n + (1 if k in ("fwd_slot_start", "cu_seqlens") else 0), dtype=torch.int32, device=dev)
             for k in ("order", "slot_of", "fwd_of_slot", "fwd_slot_start", "fwd_width", "cu_seqlens", "last_varlen",
@@ -281,7 +288,7 @@ def main():
         if ev:
             ev[2].record(stream)
         blink.blink_label_readout(hidden, plan["last_varlen"], W, off, ids, rd.temperature, probs=probs, ws=ws_r,
-                                  slot_of=plan["slot_of"])
+                                  slot_of=plan["slot_of"], qtype=qtype, answers=answers)
         if ev:
             ev[3].record(stream)
 
@@ -414,13 +421,15 @@ def e2e(blink, dev, w, lengths, ins, rd, flush, args, world):
     host = {"len": pinned(lengths.astype(np.int32), np.int32), "q": pinned(ins.q, np.int16),
             "kt": pinned(ins.k_tail, np.int16), "vt": pinned(ins.v_tail, np.int16),
             "hid": pinned(rd.hidden, np.int16), "off": pinned(rd.label_off, np.int32),
-            "ids": pinned(rd.label_ids, np.int32)}
+            "ids": pinned(rd.label_ids, np.int32), "qt": pinned(wl_question_types(w, rd.label_off), np.int32)}
     if ins.P:
         host["kp"] = pinned(ins.k_pre, np.int16)
         host["vp"] = pinned(ins.v_pre, np.int16)
     devb = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host.items()}
     W = torch.from_numpy(np.ascontiguousarray(rd.unembed).view(np.int16)).view(torch.bfloat16).to(dev)  # resident
     h_probs = torch.empty(len(rd.label_ids), dtype=torch.float32, pin_memory=True)
+    h_answers = torch.empty(w.n, 3, dtype=torch.float32, pin_memory=True)
+    d_answers = torch.empty(w.n, 3, dtype=torch.float32, device=dev)
     n = w.n
     plan = None
     out = torch.empty(ins.q.shape, dtype=torch.bfloat16, device=dev)
@@ -438,7 +447,8 @@ def e2e(blink, dev, w, lengths, ins, rd, flush, args, world):
                                           devb["vt"].view(bf), plan["cu_seqlens"], B=n, P=ins.P,
                                           max_tail=int(lengths.max()), out=out, ws=ws_a)
         blink.blink_label_readout(devb["hid"].view(bf), plan["last_varlen"], W, devb["off"], devb["ids"],
-                                  rd.temperature, host_probs=h_probs, ws=ws_r, slot_of=plan["slot_of"])
+                                  rd.temperature, host_probs=h_probs, ws=ws_r, slot_of=plan["slot_of"],
+                                  qtype=devb["qt"], answers=d_answers, host_answers=h_answers)
 
     for _ in range(max(2, args.warmup)):
         one()
@@ -459,7 +469,8 @@ def e2e(blink, dev, w, lengths, ins, rd, flush, args, world):
         sec = float(t.item())
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     return {"value": world * n / sec, "unit": "questions/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(h_probs.numel() * 4 + 4), "ms_per_step": sec * 1000, "steps": steps,
+            "d2h_bytes_per_step": int(h_probs.numel() * 4 + h_answers.numel() * 4 + 4), "ms_per_step": sec * 1000,
+            "steps": steps,
             "resident": "unembedding (model weight) stays on the device"}
 
 

@@ -147,7 +147,8 @@ blink_status blink_prefix_tail_attention(const blink_bf16 *q, const blink_bf16 *
 /* ------------------------------------------------------------------------------------------
  * Label readout -- blink.py `_read` / `_read_batched` (the last hidden state of each question
  * against the lm_head rows of its offered labels only, in FP32), `softmax` (z / T, minus the
- * max, exp, normalise) and `decide` (the temperature must be positive).
+ * max, exp, normalise), `decide` (the temperature must be positive) and, optionally,
+ * `answer_for` (the typed answer per question).
  *
  * hidden [hidden_rows, H] bf16, row r at hidden + r * hidden_row_stride (elements; multiple of 8)
  * d_last_idx              hidden row of each last token (0 <= idx < hidden_rows): indexed by
@@ -162,6 +163,14 @@ blink_status blink_prefix_tail_attention(const blink_bf16 *q, const blink_bf16 *
  * h_probs                 optional pinned host copy of d_probs; when given the call copies once
  *                         and synchronises the stream, and reports device-side errors
  * d_logits [sum_k]        optional fp32 raw logits (before the temperature)
+ * d_qtype [B], d_answers [B][3], h_answers   optional, together: blink.py `answer_for` on the device.
+ *                         d_qtype[b] is 0 (choice), 1 (noul: first label = "yes") or 2 (score:
+ *                         label i = level i); d_answers[b] = {index, confidence, value} as fp32:
+ *                         the chosen label (first of equal probabilities), for a choice
+ *                         (p_best - 1/K)/(1 - 1/K) and p_best, for a score the same confidence
+ *                         clamped to [0, 1] and the expected level sum_i i p_i, for a noul NaN and
+ *                         p_yes (probabilities renormalised first).  h_answers (pinned) receives a
+ *                         copy in the same synchronising host transfer as h_probs.
  * d_ws, ws_bytes          workspace of blink_label_readout_workspace(B) bytes, zero-filled before
  *                         its first use; the call leaves its counters at zero
  * A label id outside [0, V) makes that question's probabilities NaN and latches
@@ -174,7 +183,8 @@ blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hidden_row_st
                                  int32_t V, int32_t H,
                                  const int32_t *d_label_off, const int32_t *d_label_ids, int32_t B,
                                  int32_t sum_k, float temperature, float *d_probs, float *h_probs,
-                                 float *d_logits, void *d_ws, size_t ws_bytes, cudaStream_t stream);
+                                 float *d_logits, const int32_t *d_qtype, float *d_answers, float *h_answers,
+                                 void *d_ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Label readout that allocates nothing.  The pages have no counterpart: this entry point is an
@@ -185,7 +195,8 @@ blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hidden_row_st
  * start-up), and latency-critical loops that must never call cudaMalloc, which may synchronise
  * the whole device.  Such callers cannot provide the `d_ws` that blink_label_readout needs.
  *
- * Arguments and results are those of blink_label_readout without d_ws / ws_bytes.  The scratch
+ * Arguments and results are those of blink_label_readout without d_ws / ws_bytes and without the
+ * answer outputs.  The scratch
  * (an error word and one ticket per question) is a static device array of
  * 256 + 4 * BLINK_STATIC_SCRATCH_QUESTIONS bytes (128.25 KiB) that every GPU which loads this
  * library keeps until the process exits.

@@ -9,6 +9,8 @@ What each function follows on the pages is stated in the C source beside it:
   pack_plan              blink.py, `_batches` / `_padded`
   prefix_tail_attention  blink.py, PREFIX_CACHE note and `_forward_shared`
   label_readout          blink.py, `_read` / `_read_batched`, `softmax`, `decide`
+and, written here in Python because the pages keep it on the host:
+  answer                 blink.py, `answer_for`
 """
 from __future__ import annotations
 
@@ -166,3 +168,34 @@ def label_readout(hidden, last_idx, unembed, label_off, label_ids, temperature: 
     if st == 1:
         raise OracleError("readout oracle rejected its arguments")
     return logits, probs, int(st)
+
+
+QTYPE_CHOICE, QTYPE_NOUL, QTYPE_SCORE = 0, 1, 2
+
+
+def answer(qtype: int, probs) -> dict:
+    """blink.py `answer_for`, restated over one question's probabilities in request order.
+
+    The probabilities are renormalised (divided by their sum, or by 1 if it is 0).  A choice
+    answers the first label with the largest probability and a confidence of
+    (p_best - 1/K) / (1 - 1/K) (1 when K = 1); a noul answers p of its first label ("yes"); a
+    score answers the expected level sum_i i * p_i, the most probable level (ties to the lowest)
+    and the same confidence clamped to [0, 1].
+    Returns {"index", "confidence", "value"}: the chosen label, the confidence (NaN for a noul)
+    and p_best / p_yes / the expected level.
+    """
+    p = [float(x) for x in probs]
+    z = sum(p) or 1.0
+    p = [x / z for x in p]
+    K = len(p)
+    best = max(range(K), key=lambda k: (p[k], -k))  # first in request order among equals
+    if qtype == QTYPE_CHOICE:
+        conf = (p[best] - 1 / K) / (1 - 1 / K) if K > 1 else 1.0
+        return {"index": best, "confidence": conf, "value": p[best]}
+    if qtype == QTYPE_NOUL:
+        return {"index": best, "confidence": float("nan"), "value": p[0]}
+    if qtype == QTYPE_SCORE:
+        ev = sum(i * p[i] for i in range(K))
+        conf = min(1.0, max(0.0, (p[best] - 1 / K) / (1 - 1 / K))) if K > 1 else 1.0
+        return {"index": best, "confidence": conf, "value": ev}
+    raise OracleError(f"unknown question type {qtype}")

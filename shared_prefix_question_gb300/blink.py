@@ -52,7 +52,7 @@ _SIGNATURES = {
                                            _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp]),
     "blink_label_readout_workspace": (_sz, [_i32]),
     "blink_label_readout": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
-                                   _vp, _sz, _vp]),
+                                   _vp, _vp, _vp, _vp, _sz, _vp]),
     "blink_label_readout_noalloc": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _f32, _vp,
                                            _vp, _vp, _vp]),
 }
@@ -178,24 +178,29 @@ def readout_workspace_bytes(B: int) -> int:
 
 
 def blink_label_readout(hidden, last_idx, unembed, label_off, label_ids, temperature: float, probs=None,
-                        host_probs=None, logits=None, ws=None, slot_of=None, stream=None):
+                        host_probs=None, logits=None, ws=None, slot_of=None, qtype=None, answers=None,
+                        host_answers=None, stream=None):
     """hidden [rows, H] bf16, last_idx int32 (per question, or per slot with `slot_of`), unembed [V, H]
     bf16, CSR label_off [B+1] / label_ids [sum K] int32, all on the device.  Returns (probs, ws); if
     `host_probs` (pinned fp32) is given the call copies into it and synchronises."""
-    _need_cuda(hidden, last_idx, unembed, label_off, label_ids, probs, logits, slot_of)
+    _need_cuda(hidden, last_idx, unembed, label_off, label_ids, probs, logits, slot_of, qtype, answers)
     rows, H = hidden.shape
     V = unembed.shape[0]
     B = label_off.numel() - 1
     sum_k = label_ids.numel()
     if probs is None:
         probs = torch.empty(sum_k, dtype=torch.float32, device=hidden.device)
+    if qtype is not None and answers is None:
+        answers = torch.empty(B, 3, dtype=torch.float32, device=hidden.device)
     if ws is None:
         ws = new_workspace(readout_workspace_bytes(B), hidden.device)
     st = lib().blink_label_readout(_ptr(hidden), int(hidden.stride(0)), int(rows), _ptr(last_idx), _ptr(slot_of), _ptr(unembed),
                                    int(V), int(H), _ptr(label_off), _ptr(label_ids), int(B), int(sum_k),
-                                   float(temperature), _ptr(probs), _ptr(host_probs), _ptr(logits), _ptr(ws),
-                                   ws.numel(), _stream(stream))
+                                   float(temperature), _ptr(probs), _ptr(host_probs), _ptr(logits), _ptr(qtype),
+                                   _ptr(answers), _ptr(host_answers), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "blink_label_readout")
+    if answers is not None:
+        return probs, ws, answers
     return probs, ws
 
 

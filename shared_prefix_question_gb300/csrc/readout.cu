@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kReadoutWarps * 32)
                    const uint16_t *__restrict__ unembed, int V, int H,
                    const int32_t *__restrict__ label_off, const int32_t *__restrict__ label_ids, int B, int sum_k,
                    float log2e_over_t, float *__restrict__ probs, float *__restrict__ logits,
+                   const int32_t *__restrict__ qtype, float *__restrict__ answers,
                    uint32_t *__restrict__ counters, int *__restrict__ err)
 {
     const int warp = threadIdx.x >> 5;
@@ -125,14 +126,13 @@ __global__ void __launch_bounds__(kReadoutWarps * 32)
         probs[r] = z;  // staged here until the question's softmax
         if (logits) logits[r] = z;
         if (bad) atomicCAS(err, 0, BLINK_DEVICE_FLAG);
-        __threadfence();
-        ticket = atomicInc(counters + b, static_cast<uint32_t>(K - 1));  // wraps back to 0 on the last
+        asm volatile("atom.release.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(ticket) : "l"(counters + b), "r"(static_cast<uint32_t>(K - 1)) : "memory");
     }
     ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
     if (ticket != static_cast<uint32_t>(K - 1)) return;
 
     // This warp completed question b: temperature softmax over its K staged logits.
-    __threadfence();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     float v[8];
     float m = -INFINITY;
 #pragma unroll
@@ -158,6 +158,59 @@ __global__ void __launch_bounds__(kReadoutWarps * 32)
         const int k = lo + lane + 32 * j;
         if (k < hi) probs[k] = v[j] * inv;
     }
+    if (qtype && answers) {
+        // blink.py `answer_for`: renormalise, then the question type's answer.
+        const int qt = __ldg(qtype + b);
+        float z = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) z += v[j] * inv;  // entries past the question are 0
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+        const float rz = z > 0.f ? 1.0f / z : 1.0f;
+        float best = -1.f, ev = 0.f;
+        int best_k = 0x7FFFFFFF;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int kl = lane + 32 * j;  // label index inside the question
+            if (kl < K) {
+                const float pk = v[j] * inv * rz;
+                if (pk > best) {  // increasing kl: the first of equal values stays
+                    best = pk;
+                    best_k = kl;
+                }
+                ev = fmaf(static_cast<float>(kl), pk, ev);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            const int ok = __shfl_xor_sync(0xFFFFFFFFu, best_k, o);
+            if (ob > best || (ob == best && ok < best_k)) {
+                best = ob;
+                best_k = ok;
+            }
+            ev += __shfl_xor_sync(0xFFFFFFFFu, ev, o);
+        }
+        const float p_first = __shfl_sync(0xFFFFFFFFu, v[0] * inv * rz, 0);
+        if (lane == 0) {
+            const float inv_k = 1.0f / static_cast<float>(K);
+            const float conf = K > 1 ? (best - inv_k) / (1.0f - inv_k) : 1.0f;
+            float c = conf, val = best;
+            if (qt == 1) {  // noul: p of its first label ("yes"); no confidence
+                c = __int_as_float(0x7FC00000);
+                val = p_first;
+            } else if (qt == 2) {  // score: expected level, confidence clamped to [0, 1]
+                c = fminf(1.0f, fmaxf(0.0f, conf));
+                val = ev;
+            } else if (qt != 0) {
+                atomicCAS(err, 0, BLINK_DEVICE_FLAG);
+                c = val = __int_as_float(0x7FC00000);
+            }
+            answers[3 * b + 0] = static_cast<float>(best_k);
+            answers[3 * b + 1] = c;
+            answers[3 * b + 2] = val;
+        }
+    }
 }
 
 }  // namespace
@@ -174,11 +227,13 @@ extern "C" blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hi
                                             const blink_bf16 *unembed, int32_t V, int32_t H,
                                             const int32_t *d_label_off, const int32_t *d_label_ids, int32_t B,
                                             int32_t sum_k, float temperature, float *d_probs, float *h_probs,
-                                            float *d_logits, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+                                            float *d_logits, const int32_t *d_qtype, float *d_answers,
+                                            float *h_answers, void *d_ws, size_t ws_bytes, cudaStream_t stream)
 {
     using namespace blink;
     if (!hidden || !d_last_idx || !unembed || !d_label_off || !d_label_ids || !d_probs || !d_ws)
         return BLINK_INVALID_ARG;
+    if ((d_qtype == nullptr) != (d_answers == nullptr) || (h_answers && !d_answers)) return BLINK_INVALID_ARG;
     if (!(temperature > 0.f) || !(temperature < INFINITY)) return BLINK_INVALID_ARG;  // blink.py `decide`
     if (V < 1 || H < 8 || H % 8 != 0 || hidden_rows < 1 || hidden_row_stride < H || hidden_row_stride % 8 != 0)
         return BLINK_INVALID_ARG;
@@ -196,12 +251,16 @@ extern "C" blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hi
     const float log2e_over_t = kLog2e / temperature;
     readout_kernel<<<grid, kReadoutWarps * 32, 0, stream>>>(hidden, hidden_row_stride, hidden_rows, d_last_idx,
                                                            d_slot_of, unembed, V, H, d_label_off, d_label_ids, B, sum_k,
-                                                           log2e_over_t, d_probs, d_logits, counters, &hdr->error);
+                                                           log2e_over_t, d_probs, d_logits, d_qtype, d_answers,
+                                                           counters, &hdr->error);
     if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
-    if (h_probs) {
+    if (h_probs || h_answers) {
         int32_t word = 0;
-        if (cudaMemcpyAsync(h_probs, d_probs, static_cast<size_t>(sum_k) * sizeof(float), cudaMemcpyDeviceToHost,
-                            stream) != cudaSuccess)
+        if (h_probs && cudaMemcpyAsync(h_probs, d_probs, static_cast<size_t>(sum_k) * sizeof(float),
+                                       cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        if (h_answers && cudaMemcpyAsync(h_answers, d_answers, static_cast<size_t>(B) * 3 * sizeof(float),
+                                         cudaMemcpyDeviceToHost, stream) != cudaSuccess)
             return BLINK_CUDA_ERROR;
         if (cudaMemcpyAsync(&word, &hdr->error, sizeof word, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
             return BLINK_CUDA_ERROR;
@@ -272,8 +331,8 @@ extern "C" blink_status blink_label_readout_noalloc(const blink_bf16 *hidden, in
     const int grid = (sum_k + kReadoutWarps - 1) / kReadoutWarps;
     readout_kernel<<<grid, kReadoutWarps * 32, 0, stream>>>(hidden, hidden_row_stride, hidden_rows, d_last_idx,
                                                            d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
-                                                           sum_k, kLog2e / temperature, d_probs, d_logits, counters,
-                                                           err);
+                                                           sum_k, kLog2e / temperature, d_probs, d_logits, nullptr,
+                                                           nullptr, counters, err);
     if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
     if (h_probs) {
         int32_t word = 0;

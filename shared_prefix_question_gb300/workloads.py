@@ -213,3 +213,18 @@ def readout_inputs(w: Workload, rows: int | None = None, last_idx: np.ndarray | 
         unembed = normal_bf16(rng, (w.V, w.H), std=0.02)
     off, ids = label_csr(w)
     return ReadoutInputs(hidden, np.asarray(last_idx, dtype=np.int32), unembed, off, ids, w.temperature)
+
+
+QTYPE_CHOICE, QTYPE_NOUL, QTYPE_SCORE = 0, 1, 2
+
+
+def question_types(w: Workload, label_off: np.ndarray) -> np.ndarray:
+    """Seeded question types consistent with the label counts (blink.py `question_options`):
+    a noul offers exactly two labels (yes, no), a score 2 to 10 levels, a choice 1 to 255 options."""
+    counts = np.diff(np.asarray(label_off))
+    rng = np.random.default_rng(3000 + w.index)
+    draw = rng.integers(0, 3, size=counts.shape[0])
+    qt = np.full(counts.shape[0], QTYPE_CHOICE, dtype=np.int32)
+    qt[(counts == 2) & (draw == 1)] = QTYPE_NOUL
+    qt[(counts >= 2) & (counts <= 10) & (draw == 2)] = QTYPE_SCORE
+    return qt

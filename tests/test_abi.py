@@ -61,8 +61,8 @@ def test_readout_host_checks(lib):
     def call(**kw):
         a = dict(args, **kw)
         return L.blink_label_readout(a["hidden"], a["stride"], a["rows"], a["last"], None, a["W"], a["V"], a["H"], a["off"],
-                                     a["ids"], a["B"], a["sum_k"], a["T"], a["probs"], a["hp"], a["logits"], a["ws"],
-                                     a["wsb"], a["stream"])
+                                     a["ids"], a["B"], a["sum_k"], a["T"], a["probs"], a["hp"], a["logits"], a.get("qt"),
+                                     a.get("ans"), a.get("hans"), a["ws"], a["wsb"], a["stream"])
     for t in (0.0, -0.5, float("inf"), float("nan")):     # blink.py `decide`: temperature must be positive
         assert call(T=t) == blink.BLINK_INVALID_ARG
     assert call(H=100) == blink.BLINK_INVALID_ARG         # not a multiple of 8
@@ -71,6 +71,8 @@ def test_readout_host_checks(lib):
     assert call(B=2, sum_k=2 * 255 + 1) == blink.BLINK_OUT_OF_RANGE  # more than MAX_OPTIONS per question
     assert call(wsb=16) == blink.BLINK_WORKSPACE_TOO_SMALL
     assert call(probs=None) == blink.BLINK_INVALID_ARG
+    assert call(qt=FAKE) == blink.BLINK_INVALID_ARG          # question types without an answers buffer
+    assert call(hans=FAKE) == blink.BLINK_INVALID_ARG        # host answers without device answers
 
 
 def test_attention_host_checks(lib):

@@ -99,3 +99,43 @@ def test_readout_repeated_calls_reuse_workspace():
         probs, ws = blink.blink_label_readout(hidden, last, W, off, ids, 1.0, ws=ws)
         torch.cuda.synchronize()
         compare_readout(probs.cpu().numpy().astype(np.float64), ins)
+
+
+@pytest.mark.parametrize("name", ["tiny", "18k", "max"])
+def test_readout_answers(name):
+    """blink.py `answer_for` on the device, fused into the readout, against the oracle's answers
+    computed from the oracle's probabilities."""
+    from oracle import oracle
+    from tests.helpers import ARGMAX_TIE_GAP
+    w = wl.WORKLOADS[name]
+    ins = wl.readout_inputs(w, unembed=None if name == "tiny" else _unembed(w))
+    qt = wl.question_types(w, ins.label_off)
+    hidden = dev_bf16(ins.hidden)
+    W = dev_bf16(ins.unembed)
+    hp = torch.empty(len(ins.label_ids), dtype=torch.float32, pin_memory=True)
+    ha = torch.empty(len(ins.last_idx), 3, dtype=torch.float32, pin_memory=True)
+    probs, ws, answers = blink.blink_label_readout(hidden, dev_i32(ins.last_idx), W, dev_i32(ins.label_off),
+                                                   dev_i32(ins.label_ids), ins.temperature, host_probs=hp,
+                                                   qtype=dev_i32(qt), host_answers=ha)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(answers.cpu().numpy(), ha.numpy())
+    z, p_ref, st = oracle.label_readout(ins.hidden, ins.last_idx, ins.unembed, ins.label_off, ins.label_ids,
+                                        ins.temperature)
+    got = ha.numpy().astype(np.float64)
+    for b in range(len(ins.last_idx)):
+        lo, hi = ins.label_off[b], ins.label_off[b + 1]
+        ref = oracle.answer(int(qt[b]), p_ref[lo:hi])
+        zb = z[lo:hi]
+        top = np.argsort(-zb, kind="stable")
+        near_tie = hi - lo >= 2 and zb[top[0]] - zb[top[1]] < ARGMAX_TIE_GAP
+        if near_tie:
+            assert int(got[b, 0]) in (int(top[0]), int(top[1]))
+        else:
+            assert int(got[b, 0]) == ref["index"], b
+            K = hi - lo
+            tol = 1e-3 * max(1, K) if qt[b] == wl.QTYPE_SCORE else 1e-3
+            if np.isnan(ref["confidence"]):
+                assert np.isnan(got[b, 1])
+            else:
+                assert abs(got[b, 1] - ref["confidence"]) <= 2e-3
+            assert abs(got[b, 2] - ref["value"]) <= tol
