@@ -99,6 +99,39 @@ blink_status blink_pack_plan(const int32_t *d_lengths, int32_t n, int32_t budget
                              cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Shared-prefix length -- blink.py `_shared_prefix_len`: the number of leading tokens common to
+ * every sequence, leaving each sequence at least one token of its own (its answer position is
+ * computed in the per-question pass); 0 for fewer than two sequences.  blink.py `_forward` takes
+ * the shared path only when this is at least PREFIX_MIN_TOKENS (256), a host decision.
+ *
+ * d_tokens, n_tokens  int32 token ids of all sequences back to back (n_tokens of them); sequence i
+ *                     at d_tokens + (d_cu[i] - d_cu[0]) with length d_cu[i+1] - d_cu[i] (>= 1)
+ * d_cu [n+1], n       1..BLINK_MAX_PLAN_SEQUENCES sequences
+ * d_len [1]           output (device); h_len optional pinned host copy (the call then synchronises)
+ * d_ws, ws_bytes      workspace of blink_shared_prefix_len_workspace() bytes (error word)
+ * A length below 1 or a sequence past n_tokens latches BLINK_DEVICE_FLAG.
+ * ------------------------------------------------------------------------------------------ */
+size_t blink_shared_prefix_len_workspace(void);
+
+blink_status blink_shared_prefix_len(const int32_t *d_tokens, int64_t n_tokens, const int32_t *d_cu, int32_t n,
+                                     int32_t *d_len, int32_t *h_len, void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * KV rows into the arena -- simit engine.py: one contiguous KV arena with a region per request
+ * (`KVArena`, `arena.copy`): the prefix's K/V, computed once, are written into its region, and a
+ * cached prefix region can be copied into another request's region.
+ *
+ * Copies n_rows token rows of row_elems (= Hkv * d, a multiple of 8) bf16 values, for K and V,
+ * from k_src / v_src (rows src_row_stride elements apart) to arena rows
+ * [dst_slot, dst_slot + n_rows) (rows arena_row_stride elements apart, arena_slots rows in all).
+ * Source and destination must not overlap.  Asynchronous on `stream`.
+ * Errors: BLINK_INVALID_ARG (null, alignment, strides), BLINK_OUT_OF_RANGE (rows past the arena).
+ * ------------------------------------------------------------------------------------------ */
+blink_status blink_kv_to_arena(const blink_bf16 *k_src, const blink_bf16 *v_src, int64_t src_row_stride,
+                               int64_t n_rows, int32_t row_elems, blink_bf16 *k_arena, blink_bf16 *v_arena,
+                               int64_t arena_row_stride, int64_t arena_slots, int64_t dst_slot, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Prefix-tail attention -- blink.py PREFIX_CACHE note and `_forward_shared` (the prefix is
  * encoded once; every tail runs against it: same tokens, same positions, only the
  * floating-point order differs), with the arena layout of simit engine.py.
@@ -143,6 +176,31 @@ blink_status blink_prefix_tail_attention(const blink_bf16 *q, const blink_bf16 *
                                          int32_t max_tail, int32_t Hq, int32_t Hkv, int32_t d, float scale,
                                          blink_bf16 *out, float *lse, void *d_ws, size_t ws_bytes,
                                          cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Prefix-tail attention over several requests in one launch -- blink.py `logits_many` /
+ * `Batcher` (every question of up to 64 requests packed into the same forwards, each request's
+ * rows taken only from its own prompts) with simit engine.py's arena (one arena, a region per
+ * request).  Request r owns the tail rows [h_req_rows[r], h_req_rows[r+1]) (whole questions
+ * only) and attends to its own prefix of h_req_prefix_len[r] tokens at arena slots
+ * [h_req_prefix_start[r], + h_req_prefix_len[r]).  Per row the result is exactly that of
+ * blink_prefix_tail_attention with the request's prefix.
+ *
+ * k_arena, v_arena  [arena_slots, Hkv, d] bf16 rows arena_row_stride elements apart
+ * n_req             1..64
+ * h_req_rows        host [n_req+1], h_req_rows[0] = 0, non-decreasing, h_req_rows[n_req] = rows
+ * h_req_prefix_*    host [n_req]; a request with prefix length 0 runs the plain causal path
+ * Other arguments and errors as blink_prefix_tail_attention; a question that starts before its
+ * request's first row latches BLINK_DEVICE_FLAG.
+ * ------------------------------------------------------------------------------------------ */
+blink_status blink_prefix_tail_attention_multi(const blink_bf16 *q, const blink_bf16 *k_arena, const blink_bf16 *v_arena,
+                                               int64_t arena_row_stride, int64_t arena_slots, const blink_bf16 *k_tail,
+                                               const blink_bf16 *v_tail, const int32_t *d_cu_seqlens,
+                                               const int32_t *d_seq_start, int32_t B, int32_t rows, int32_t n_req,
+                                               const int32_t *h_req_rows, const int32_t *h_req_prefix_start,
+                                               const int32_t *h_req_prefix_len, int32_t max_tail, int32_t Hq,
+                                               int32_t Hkv, int32_t d, float scale, blink_bf16 *out, float *lse,
+                                               void *d_ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Label readout -- blink.py `_read` / `_read_batched` (the last hidden state of each question

@@ -9,8 +9,9 @@ What each function follows on the pages is stated in the C source beside it:
   pack_plan              blink.py, `_batches` / `_padded`
   prefix_tail_attention  blink.py, PREFIX_CACHE note and `_forward_shared`
   label_readout          blink.py, `_read` / `_read_batched`, `softmax`, `decide`
-and, written here in Python because the pages keep it on the host:
+and, written here in Python because the pages keep them on the host:
   answer                 blink.py, `answer_for`
+  shared_prefix_len      blink.py, `_shared_prefix_len`
 """
 from __future__ import annotations
 
@@ -199,3 +200,18 @@ def answer(qtype: int, probs) -> dict:
         conf = min(1.0, max(0.0, (p[best] - 1 / K) / (1 - 1 / K))) if K > 1 else 1.0
         return {"index": best, "confidence": conf, "value": ev}
     raise OracleError(f"unknown question type {qtype}")
+
+
+def shared_prefix_len(seqs) -> int:
+    """blink.py `_shared_prefix_len`, as the page states it: with fewer than two sequences, 0;
+    otherwise the common prefix of the lexicographically smallest and largest sequences (which
+    is the common prefix of all of them), clipped so every sequence keeps at least one token."""
+    seqs = [list(map(int, s)) for s in seqs]
+    if len(seqs) < 2:
+        return 0
+    lo, hi = min(seqs), max(seqs)
+    n = min(len(lo), len(hi))
+    p = 0
+    while p < n and lo[p] == hi[p]:
+        p += 1
+    return min(p, min(len(s) for s in seqs) - 1)

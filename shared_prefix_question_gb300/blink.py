@@ -50,6 +50,11 @@ _SIGNATURES = {
     "blink_attention_workspace": (_sz, [_i32] * 6),
     "blink_prefix_tail_attention": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                            _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "blink_prefix_tail_attention_multi": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp,
+                                                 _vp, _vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "blink_shared_prefix_len_workspace": (_sz, []),
+    "blink_shared_prefix_len": (_i32, [_vp, _i64, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "blink_kv_to_arena": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _i64, _i64, _i64, _vp]),
     "blink_label_readout_workspace": (_sz, [_i32]),
     "blink_label_readout": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
                                    _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -168,6 +173,40 @@ def blink_prefix_tail_attention(q, k_pre, v_pre, k_tail, v_tail, cu_seqlens, B: 
     return out, lse, ws
 
 
+def blink_prefix_tail_attention_multi(q, k_arena, v_arena, k_tail, v_tail, cu_seqlens, B: int, req_rows,
+                                      req_prefix_start, req_prefix_len, max_tail: int, seq_start=None,
+                                      scale: float = 0.0, out=None, lse=None, want_lse: bool = False, ws=None,
+                                      arena_row_stride: int | None = None, stream=None):
+    """Several requests in one launch: request r owns rows [req_rows[r], req_rows[r+1]) of q/k_tail/
+    v_tail and attends to arena slots [req_prefix_start[r], + req_prefix_len[r]).  The arena tensors
+    are [slots, Hkv, d] (or [slots, stride] with `arena_row_stride`).  Returns (out, lse, ws)."""
+    import numpy as np
+    _need_cuda(q, k_tail, v_tail, cu_seqlens, seq_start)
+    rows, Hq, d = q.shape
+    Hkv = k_tail.shape[1]
+    n_req = len(req_prefix_len)
+    h_rows = np.ascontiguousarray(req_rows, dtype=np.int32)
+    h_start = np.ascontiguousarray(req_prefix_start, dtype=np.int32)
+    h_len = np.ascontiguousarray(req_prefix_len, dtype=np.int32)
+    if arena_row_stride is None:
+        arena_row_stride = Hkv * d
+    slots = int(k_arena.shape[0]) if k_arena is not None else 0
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(Hq, rows, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = new_workspace(attention_workspace_bytes(rows, B, 0, Hq, Hkv, d), q.device)
+    st = lib().blink_prefix_tail_attention_multi(
+        _ptr(q), _ptr(k_arena), _ptr(v_arena), int(arena_row_stride), slots,
+        _ptr(k_tail), _ptr(v_tail), _ptr(cu_seqlens), _ptr(seq_start), int(B), int(rows), int(n_req),
+        h_rows.ctypes.data_as(ctypes.c_void_p), h_start.ctypes.data_as(ctypes.c_void_p),
+        h_len.ctypes.data_as(ctypes.c_void_p), int(max_tail), int(Hq), int(Hkv), int(d), float(scale), _ptr(out),
+        _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "blink_prefix_tail_attention_multi")
+    return out, lse, ws
+
+
 def blink_read_device_status(ws: torch.Tensor, clear: bool = True, stream=None) -> int:
     return int(lib().blink_read_device_status(_ptr(ws), 1 if clear else 0, _stream(stream)))
 
@@ -225,3 +264,30 @@ def blink_label_readout_noalloc(hidden, last_idx, unembed, label_off, label_ids,
                                            _ptr(host_probs), _ptr(logits), _stream(stream))
     _check(st, "blink_label_readout_noalloc")
     return probs
+
+
+# ------------------------------------------------------------------------------------------------ prefix side
+def blink_shared_prefix_len(tokens, cu, out=None, sync: bool = True, ws=None, stream=None):
+    """Shared-prefix length of the sequences in `tokens` (int32, back to back, offsets `cu`)."""
+    _need_cuda(tokens, cu)
+    n = cu.numel() - 1
+    if out is None:
+        out = torch.empty(1, dtype=torch.int32, device=tokens.device)
+    if ws is None:
+        ws = new_workspace(int(lib().blink_shared_prefix_len_workspace()), tokens.device)
+    host = torch.empty(1, dtype=torch.int32, pin_memory=True) if sync else None
+    st = lib().blink_shared_prefix_len(_ptr(tokens), int(tokens.numel()), _ptr(cu), int(n), _ptr(out), _ptr(host),
+                                       _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "blink_shared_prefix_len")
+    return int(host.item()) if sync else out
+
+
+def blink_kv_to_arena(k_src, v_src, k_arena, v_arena, dst_slot: int, stream=None):
+    """Write the token rows of k_src / v_src ([n, ...] bf16, rows contiguous) into arena rows
+    [dst_slot, dst_slot + n) of k_arena / v_arena ([slots, stride] bf16)."""
+    n = k_src.shape[0]
+    row_elems = k_src[0].numel() if n else 0
+    st = lib().blink_kv_to_arena(_ptr(k_src), _ptr(v_src), int(k_src.stride(0)), int(n), int(row_elems),
+                                 _ptr(k_arena), _ptr(v_arena), int(k_arena.stride(0)), int(k_arena.shape[0]),
+                                 int(dst_slot), _stream(stream))
+    _check(st, "blink_kv_to_arena")

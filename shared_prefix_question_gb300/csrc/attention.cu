@@ -42,14 +42,24 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 constexpr uint32_t kTmemCols = 512;
 
+constexpr int kMaxRequests = 64;  // blink.py `Batcher.MAX_REQUESTS`
+
 struct AttnArgs {
     const int32_t *cu;         // [B+1]
     const int32_t *seq_start;  // [B] or nullptr (varlen)
     uint16_t *out;             // [rows, Hq, D]
     float *lse;                // [Hq, rows] or nullptr
     int *err;
-    int rows, B, P, Hq, Hkv, g, tpt, n_pre, max_tail;
+    int rows, B, Hq, Hkv, g, tpt, max_tail;
     float scale_log2;
+    // Requests: request r owns tail rows [req_row[r], req_row[r+1]) and the prefix of req_P[r]
+    // tokens at arena slots [req_pre[r], req_pre[r] + req_P[r]).  Blocks [req_blk[r], req_blk[r+1])
+    // work on request r (a block never straddles two requests).
+    int n_req;
+    int req_row[kMaxRequests + 1];
+    int req_blk[kMaxRequests + 1];
+    int req_pre[kMaxRequests];
+    int req_P[kMaxRequests];
 };
 
 template <int D>
@@ -119,7 +129,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int head = blockIdx.y;
-    const int t0 = blockIdx.x * 2 * a.tpt;
+    int req = 0;  // this block's request
+    while (req + 1 < a.n_req && a.req_blk[req + 1] <= static_cast<int>(blockIdx.x)) ++req;
+    const int req_begin = a.req_row[req], req_end = a.req_row[req + 1];
+    const int P = a.req_P[req], pre_start = a.req_pre[req];
+    const int n_pre = (P + BN - 1) / BN;
+    const int t0 = req_begin + (static_cast<int>(blockIdx.x) - a.req_blk[req]) * 2 * a.tpt;
 
     if (threadIdx.x == kProducerWarp * 32) {
         ptx::mbar_init(q_full, 1);
@@ -135,12 +150,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(mma_done, 1);
         ptx::fence_mbar_init();
         // Tail keys this block needs: from the start of the first question it touches.
-        const int t_end = min(t0 + 2 * a.tpt, a.rows);
+        const int t_end = min(t0 + 2 * a.tpt, req_end);
         int kbeg = -1;
         int b = owner_floor(a, t0);
         if (b >= 0) {
             const int s = start_of(a, b), len = len_of(a, b);
-            if (!question_ok(a, s, len)) atomicCAS(a.err, 0, BLINK_DEVICE_FLAG);
+            if (!question_ok(a, s, len) || (t0 < s + len && s < req_begin)) atomicCAS(a.err, 0, BLINK_DEVICE_FLAG);
             else if (t0 < s + len) kbeg = s;
         }
         if (kbeg < 0 && b + 1 < a.B) {
@@ -182,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t tmem = *tmem_holder;
     const int kbeg = sched[0];
-    const int n_iter = a.n_pre + sched[1];
+    const int n_iter = n_pre + sched[1];
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------------- TMA producer
@@ -191,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The second tile is loaded only if it starts inside the tensor (its rows past the end
             // are then zero-filled by the copy); otherwise its rows stay as they are and are never
             // stored.
-            const int q_tiles = (t0 + a.tpt < a.rows) ? 2 : 1;
+            const int q_tiles = (t0 + a.tpt < req_end) ? 2 : 1;
             int n = 0;
             ptx::mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(q_tiles) * L::kPanels * q_box);
             for (int t = 0; t < q_tiles; ++t)
@@ -199,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_3d((t == 0 ? q_s0 : q_s1) + p * kHalfBytes, &tm_q, p * 64, head * a.g,
                                      t0 + t * a.tpt, q_full);
             for (int it = 0; it < n_iter; ++it) {
-                const bool pre = it < a.n_pre;
-                const int kb = pre ? it * BN : kbeg + (it - a.n_pre) * BN;
+                const bool pre = it < n_pre;
+                const int kb = pre ? pre_start + it * BN : kbeg + (it - n_pre) * BN;
                 bool ok = true;
                 for (int kv = 0; kv < 2; ++kv) {
                     const int slot = n % kSlots;
@@ -320,14 +335,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t o_col = 256u + t * D;
         const int tok = t0 + t * a.tpt + r / a.g;
         const int hq = head * a.g + r % a.g;
-        const bool row_ok = r < rows_used && tok < a.rows;
+        const bool row_ok = r < rows_used && tok < req_end;
         bool owned = false;
         int q_lo = 0;
         if (row_ok) {
             const int b = owner_floor(a, tok);
             if (b >= 0) {
                 const int s = start_of(a, b), len = len_of(a, b);
-                if (!question_ok(a, s, len)) {
+                if (!question_ok(a, s, len) || (tok < s + len && s < req_begin)) {
                     atomicCAS(a.err, 0, BLINK_DEVICE_FLAG);
                 } else if (tok < s + len) {
                     owned = true;
@@ -352,16 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < BN; ++j) s[j] = __uint_as_float(raw[j]);
             }
             // masks
-            if (i < a.n_pre) {
+            if (i < n_pre) {
                 const int kb = i * BN;
-                if (kb + BN > a.P) {
-                    const int lim = a.P - kb;
+                if (kb + BN > P) {
+                    const int lim = P - kb;
 #pragma unroll
                     for (int j = 0; j < BN; ++j)
                         if (j >= lim) s[j] = -INFINITY;
                 }
             } else {
-                const int kb = kbeg + (i - a.n_pre) * BN;
+                const int kb = kbeg + (i - n_pre) * BN;
                 const int lo_j = q_lo - kb;
                 const int hi_j = owned ? tok - kb : -1;
 #pragma unroll
@@ -459,6 +474,117 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 }  // namespace blink
 
+namespace blink {
+namespace {
+
+// Validates the common arguments, encodes the tensor maps and launches the kernel for the request
+// table already filled in `a` (n_req, req_row, req_pre, req_P).  The arena holds arena_slots
+// token rows (every request's prefix lives in it).
+blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16 *k_arena, const blink_bf16 *v_arena,
+                              int64_t arena_row_stride, int64_t arena_slots, const blink_bf16 *k_tail,
+                              const blink_bf16 *v_tail, const int32_t *d_cu_seqlens, const int32_t *d_seq_start,
+                              int32_t B, int32_t rows, int32_t max_tail, int32_t Hq, int32_t Hkv, int32_t d,
+                              float scale, blink_bf16 *out, float *lse, void *d_ws, size_t ws_bytes,
+                              cudaStream_t stream)
+{
+    if (!q || !k_tail || !v_tail || !d_cu_seqlens || !out || !d_ws) return BLINK_INVALID_ARG;
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 64 && d != 128) || rows < 1 || max_tail < 1)
+        return BLINK_INVALID_ARG;
+    const int g = Hq / Hkv;
+    if (g > BM) return BLINK_INVALID_ARG;
+    if (B < 1 || B > BLINK_MAX_PLAN_SEQUENCES) return BLINK_OUT_OF_RANGE;
+    if (max_tail > BLINK_MAX_INPUT_TOKENS) return BLINK_OUT_OF_RANGE;
+    if (a.n_req < 1 || a.n_req > kMaxRequests) return BLINK_OUT_OF_RANGE;
+    bool any_prefix = false;
+    if (a.req_row[0] != 0 || a.req_row[a.n_req] != rows) return BLINK_INVALID_ARG;
+    for (int r = 0; r < a.n_req; ++r) {
+        if (a.req_row[r + 1] < a.req_row[r]) return BLINK_INVALID_ARG;
+        if (a.req_P[r] < 0 || a.req_P[r] > BLINK_MAX_INPUT_TOKENS) return BLINK_OUT_OF_RANGE;
+        if (a.req_P[r] > 0) {
+            any_prefix = true;
+            if (a.req_pre[r] < 0 || static_cast<int64_t>(a.req_pre[r]) + a.req_P[r] > arena_slots)
+                return BLINK_INVALID_ARG;
+        } else {
+            a.req_pre[r] = 0;
+        }
+    }
+    if (any_prefix) {
+        if (!k_arena || !v_arena || arena_slots < 1 || arena_slots > 0x7FFFFFFF) return BLINK_INVALID_ARG;
+        if (arena_row_stride < static_cast<int64_t>(Hkv) * d || arena_row_stride % 8 != 0) return BLINK_INVALID_ARG;
+        if (!aligned16(k_arena) || !aligned16(v_arena)) return BLINK_INVALID_ARG;
+    }
+    if (!aligned16(q) || !aligned16(k_tail) || !aligned16(v_tail) || !aligned16(out)) return BLINK_INVALID_ARG;
+    if (ws_bytes < blink_attention_workspace(rows, B, 0, Hq, Hkv, d)) return BLINK_WORKSPACE_TOO_SMALL;
+
+    // blocks per request: pairs of M tiles of tpt tokens over the request's own rows
+    const int tpt = BM / g;
+    int64_t blocks = 0;
+    for (int r = 0; r < a.n_req; ++r) {
+        a.req_blk[r] = static_cast<int>(blocks);
+        const int64_t tiles = (static_cast<int64_t>(a.req_row[r + 1] - a.req_row[r]) + tpt - 1) / tpt;
+        blocks += (tiles + 1) / 2;
+        if (blocks > 0x7FFFFFFF) return BLINK_OUT_OF_RANGE;
+    }
+    a.req_blk[a.n_req] = static_cast<int>(blocks);
+    if (Hkv > 65535) return BLINK_OUT_OF_RANGE;
+    if (blocks == 0) return BLINK_OK;
+
+    CUtensorMap tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail;
+    const uint64_t e = 2;  // bytes per bf16
+    bool ok = encode_tmap_3d_bf16(&tm_q, q, d, Hq, rows, d * e, static_cast<uint64_t>(Hq) * d * e, 64, g, tpt);
+    ok = ok && encode_tmap_3d_bf16(&tm_ktail, k_tail, d, Hkv, rows, d * e, static_cast<uint64_t>(Hkv) * d * e, 64,
+                                   1, BN);
+    ok = ok && encode_tmap_3d_bf16(&tm_vtail, v_tail, d, Hkv, rows, d * e, static_cast<uint64_t>(Hkv) * d * e, 64,
+                                   1, BN);
+    if (any_prefix) {
+        ok = ok && encode_tmap_3d_bf16(&tm_kpre, k_arena, d, Hkv, static_cast<uint64_t>(arena_slots), d * e,
+                                       static_cast<uint64_t>(arena_row_stride) * e, 64, 1, BN);
+        ok = ok && encode_tmap_3d_bf16(&tm_vpre, v_arena, d, Hkv, static_cast<uint64_t>(arena_slots), d * e,
+                                       static_cast<uint64_t>(arena_row_stride) * e, 64, 1, BN);
+    } else {
+        tm_kpre = tm_ktail;  // never read: no prefix tiles
+        tm_vpre = tm_vtail;
+    }
+    if (!ok) return BLINK_CUDA_ERROR;
+
+    a.cu = d_cu_seqlens;
+    a.seq_start = d_seq_start;
+    a.out = out;
+    a.lse = lse;
+    a.err = &static_cast<WorkspaceHeader *>(d_ws)->error;
+    a.rows = rows;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.g = g;
+    a.tpt = tpt;
+    a.max_tail = max_tail;
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
+    a.scale_log2 = sc * kLog2e;
+
+    dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(Hkv));
+    if (d == 128) {
+        const int smem = Layout<128>::kAlloc;
+        if (cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        attention_kernel<128><<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
+    } else {
+        // Reserve enough shared memory that only one block fits per SM: each block takes all
+        // 512 tensor-memory columns.
+        const int smem = Layout<64>::kAlloc > 120 * 1024 ? Layout<64>::kAlloc : 120 * 1024;
+        if (cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        attention_kernel<64><<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
+    }
+    if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+    return BLINK_OK;
+}
+
+}  // namespace
+}  // namespace blink
+
 extern "C" size_t blink_attention_workspace(int32_t rows, int32_t B, int32_t P, int32_t Hq, int32_t Hkv, int32_t d)
 {
     (void)rows;
@@ -479,78 +605,36 @@ extern "C" blink_status blink_prefix_tail_attention(const blink_bf16 *q, const b
                                                     void *d_ws, size_t ws_bytes, cudaStream_t stream)
 {
     using namespace blink;
-    if (!q || !k_tail || !v_tail || !d_cu_seqlens || !out || !d_ws) return BLINK_INVALID_ARG;
-    if (P < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 64 && d != 128) || rows < 1 || max_tail < 1)
-        return BLINK_INVALID_ARG;
-    const int g = Hq / Hkv;
-    if (g > BM) return BLINK_INVALID_ARG;
-    if (B < 1 || B > BLINK_MAX_PLAN_SEQUENCES) return BLINK_OUT_OF_RANGE;
-    if (P > BLINK_MAX_INPUT_TOKENS || max_tail > BLINK_MAX_INPUT_TOKENS) return BLINK_OUT_OF_RANGE;
-    if (P > 0) {
-        if (!k_pre || !v_pre) return BLINK_INVALID_ARG;
-        if (pre_row_stride < static_cast<int64_t>(Hkv) * d || pre_row_stride % 8 != 0) return BLINK_INVALID_ARG;
-        if (!aligned16(k_pre) || !aligned16(v_pre)) return BLINK_INVALID_ARG;
-    }
-    if (!aligned16(q) || !aligned16(k_tail) || !aligned16(v_tail) || !aligned16(out)) return BLINK_INVALID_ARG;
-    if (ws_bytes < blink_attention_workspace(rows, B, P, Hq, Hkv, d)) return BLINK_WORKSPACE_TOO_SMALL;
-
-    const int tpt = BM / g;
-    const int64_t tiles = (static_cast<int64_t>(rows) + tpt - 1) / tpt;
-    const int64_t pairs = (tiles + 1) / 2;
-    if (pairs > 0x7FFFFFFF || Hkv > 65535) return BLINK_OUT_OF_RANGE;
-
-    CUtensorMap tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail;
-    const uint64_t e = 2;  // bytes per bf16
-    bool ok = encode_tmap_3d_bf16(&tm_q, q, d, Hq, rows, d * e, static_cast<uint64_t>(Hq) * d * e, 64, g, tpt);
-    ok = ok && encode_tmap_3d_bf16(&tm_ktail, k_tail, d, Hkv, rows, d * e, static_cast<uint64_t>(Hkv) * d * e, 64,
-                                   1, BN);
-    ok = ok && encode_tmap_3d_bf16(&tm_vtail, v_tail, d, Hkv, rows, d * e, static_cast<uint64_t>(Hkv) * d * e, 64,
-                                   1, BN);
-    if (P > 0) {
-        ok = ok && encode_tmap_3d_bf16(&tm_kpre, k_pre, d, Hkv, P, d * e, static_cast<uint64_t>(pre_row_stride) * e,
-                                       64, 1, BN);
-        ok = ok && encode_tmap_3d_bf16(&tm_vpre, v_pre, d, Hkv, P, d * e, static_cast<uint64_t>(pre_row_stride) * e,
-                                       64, 1, BN);
-    } else {
-        tm_kpre = tm_ktail;  // never read: no prefix tiles
-        tm_vpre = tm_vtail;
-    }
-    if (!ok) return BLINK_CUDA_ERROR;
-
+    if (P < 0) return BLINK_INVALID_ARG;
+    if (P > BLINK_MAX_INPUT_TOKENS) return BLINK_OUT_OF_RANGE;
+    if (rows < 1) return BLINK_INVALID_ARG;
     AttnArgs a;
-    a.cu = d_cu_seqlens;
-    a.seq_start = d_seq_start;
-    a.out = out;
-    a.lse = lse;
-    a.err = &static_cast<WorkspaceHeader *>(d_ws)->error;
-    a.rows = rows;
-    a.B = B;
-    a.P = P;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.g = g;
-    a.tpt = tpt;
-    a.n_pre = (P + BN - 1) / BN;
-    a.max_tail = max_tail;
-    const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
-    a.scale_log2 = sc * kLog2e;
+    a.n_req = 1;
+    a.req_row[0] = 0;
+    a.req_row[1] = rows;
+    a.req_pre[0] = 0;
+    a.req_P[0] = P;
+    return launch_attention(a, q, k_pre, v_pre, pre_row_stride, P, k_tail, v_tail, d_cu_seqlens, d_seq_start, B, rows,
+                            max_tail, Hq, Hkv, d, scale, out, lse, d_ws, ws_bytes, stream);
+}
 
-    dim3 grid(static_cast<unsigned>(pairs), static_cast<unsigned>(Hkv));
-    if (d == 128) {
-        const int smem = Layout<128>::kAlloc;
-        if (cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return BLINK_CUDA_ERROR;
-        attention_kernel<128><<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
-    } else {
-        // Reserve enough shared memory that only one block fits per SM: each block takes all
-        // 512 tensor-memory columns.
-        const int smem = Layout<64>::kAlloc > 120 * 1024 ? Layout<64>::kAlloc : 120 * 1024;
-        if (cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return BLINK_CUDA_ERROR;
-        attention_kernel<64><<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
+extern "C" blink_status blink_prefix_tail_attention_multi(
+    const blink_bf16 *q, const blink_bf16 *k_arena, const blink_bf16 *v_arena, int64_t arena_row_stride,
+    int64_t arena_slots, const blink_bf16 *k_tail, const blink_bf16 *v_tail, const int32_t *d_cu_seqlens,
+    const int32_t *d_seq_start, int32_t B, int32_t rows, int32_t n_req, const int32_t *h_req_rows,
+    const int32_t *h_req_prefix_start, const int32_t *h_req_prefix_len, int32_t max_tail, int32_t Hq, int32_t Hkv,
+    int32_t d, float scale, blink_bf16 *out, float *lse, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    using namespace blink;
+    if (!h_req_rows || !h_req_prefix_start || !h_req_prefix_len) return BLINK_INVALID_ARG;
+    if (n_req < 1 || n_req > kMaxRequests) return BLINK_OUT_OF_RANGE;
+    AttnArgs a;
+    a.n_req = n_req;
+    for (int r = 0; r <= n_req; ++r) a.req_row[r] = h_req_rows[r];
+    for (int r = 0; r < n_req; ++r) {
+        a.req_pre[r] = h_req_prefix_start[r];
+        a.req_P[r] = h_req_prefix_len[r];
     }
-    if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
-    return BLINK_OK;
+    return launch_attention(a, q, k_arena, v_arena, arena_row_stride, arena_slots, k_tail, v_tail, d_cu_seqlens,
+                            d_seq_start, B, rows, max_tail, Hq, Hkv, d, scale, out, lse, d_ws, ws_bytes, stream);
 }

@@ -115,3 +115,51 @@ def test_attention_workloads(name, n_sample):
     # every owned row finite (the sampled check covers values; this covers the rest)
     rows = np.concatenate([np.arange(s, s + L) for s, L in zip(ins.seq_start, ins.seq_len)])
     assert np.isfinite(out[rows]).all()
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 2, 128), (10, 2, 128), (4, 2, 64)])
+def test_attention_several_requests_one_launch(Hq, Hkv, d):
+    """blink.py `logits_many` packs the questions of several requests into one forward; each
+    request keeps its own prefix (a region of one KV arena, simit engine.py).  Every request's
+    rows must equal the single-request oracle over that request's prefix."""
+    from tests.helpers import dev_i32, host_f64
+    rng = np.random.default_rng(Hq * 7 + d)
+    reqs = [  # (prefix length, tail lengths)
+        (300, [17, 5, 40]),
+        (0, [33, 2]),        # a request on the plain causal path
+        (129, [1, 64, 9, 12]),
+        (1000, [90]),
+    ]
+    stride = Hkv * d + 64
+    starts, slot = [], 7
+    for P, _ in reqs:
+        starts.append(slot)
+        slot += P + 13
+    slots = slot
+    arena_k = wl.normal_bf16(rng, (slots, stride))
+    arena_v = wl.normal_bf16(rng, (slots, stride))
+    lengths = [L for _, tails in reqs for L in tails]
+    rows = int(sum(lengths))
+    q = wl.normal_bf16(rng, (rows, Hq, d))
+    kt = wl.normal_bf16(rng, (rows, Hkv, d))
+    vt = wl.normal_bf16(rng, (rows, Hkv, d))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    req_rows = [0]
+    for _, tails in reqs:
+        req_rows.append(req_rows[-1] + sum(tails))
+    out, lse, ws = blink.blink_prefix_tail_attention_multi(
+        dev_bf16(q), dev_bf16(arena_k), dev_bf16(arena_v), dev_bf16(kt), dev_bf16(vt), dev_i32(cu), B=len(lengths),
+        req_rows=req_rows, req_prefix_start=starts, req_prefix_len=[P for P, _ in reqs], max_tail=max(lengths),
+        want_lse=True, arena_row_stride=stride)
+    torch.cuda.synchronize()
+    assert blink.blink_read_device_status(ws) == blink.BLINK_OK
+    out, lse = host_f64(out), host_f64(lse)
+    qi = 0
+    for (P, tails), s0, r0, r1 in zip(reqs, starts, req_rows[:-1], req_rows[1:]):
+        kp = arena_k[s0:s0 + P, :Hkv * d].reshape(P, Hkv, d).copy()
+        vp = arena_v[s0:s0 + P, :Hkv * d].reshape(P, Hkv, d).copy()
+        sub = wl.AttentionInputs(q[r0:r1], kp, vp, kt[r0:r1], vt[r0:r1],
+                                 (cu[qi:qi + len(tails)] - r0).astype(np.int32), np.array(tails, dtype=np.int32),
+                                 (cu[qi:qi + len(tails) + 1] - r0).astype(np.int32), r1 - r0, P, Hq, Hkv, d)
+        compare_attention(sub, out[r0:r1], lse[:, r0:r1])
+        qi += len(tails)
