@@ -245,6 +245,40 @@ blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hidden_row_st
                                  void *d_ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Log-space readout over several option orders -- the ruling engine (engine.py `_score_plain`,
+ * `_prior`, `answer`): each question is scored in passes, one per order of its options; per
+ * pass the answer codes' logits z (from blink_label_readout's d_logits) give
+ *   lp_j = z_j - logsumexp(z) - prior_K[j]          (position j of the pass)
+ * and option i's raw score is the mean of lp over the passes, taken at the position each pass
+ * showed option i in.  Then p = softmax(raw / T) and, optionally, the typed answer (as in
+ * blink_label_readout).
+ *
+ * d_logits [..]          pass p's K logits at d_logits[d_pass_off[p] .. d_pass_off[p+1])
+ * d_key_of_pos [..]      same layout: the option index (0..K-1) pass p shows at each position;
+ *                        each pass's entries must be a permutation of 0..K-1
+ * n_pass, d_pass_off [n_pass+1]
+ * d_question_pass [B+1]  question q's passes are [d_question_pass[q], d_question_pass[q+1]) (>= 1)
+ * d_raw_off [B+1], sum_k question q's options at [d_raw_off[q], d_raw_off[q+1]) of d_raw/d_probs;
+ *                        every pass of q has that many positions (1..255)
+ * d_prior                optional [255][255] fp32: row K-1 holds the content-free log-probability
+ *                        of each position for K options (NULL: no prior subtracted)
+ * temperature            > 0 and finite
+ * d_raw [sum_k]          optional output: the mean debiased log-probabilities
+ * d_probs [sum_k]        output: softmax(raw / T); h_probs optional pinned copy
+ * d_qtype, d_answers, h_answers  optional typed answers, as for blink_label_readout
+ * d_ws, ws_bytes         blink_rotation_debias_workspace() bytes (error word)
+ * A malformed table (a pass of the wrong size, an option index out of range) latches
+ * BLINK_DEVICE_FLAG and makes that question's probabilities NaN.
+ * ------------------------------------------------------------------------------------------ */
+size_t blink_rotation_debias_workspace(void);
+
+blink_status blink_rotation_debias(const float *d_logits, const int32_t *d_pass_off, const int32_t *d_key_of_pos,
+                                   int32_t n_pass, const int32_t *d_question_pass, const int32_t *d_raw_off, int32_t B,
+                                   int32_t sum_k, const float *d_prior, float temperature, float *d_raw,
+                                   float *d_probs, float *h_probs, const int32_t *d_qtype, float *d_answers,
+                                   float *h_answers, void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Label readout that allocates nothing.  The pages have no counterpart: this entry point is an
  * addition of this library for callers that cannot hand it a workspace.
  *

@@ -12,6 +12,7 @@ What each function follows on the pages is stated in the C source beside it:
 and, written here in Python because the pages keep them on the host:
   answer                 blink.py, `answer_for`
   shared_prefix_len      blink.py, `_shared_prefix_len`
+  rotation_debias        ruling engine.py, `_score_plain` / `_prior` / `answer`
 """
 from __future__ import annotations
 
@@ -215,3 +216,35 @@ def shared_prefix_len(seqs) -> int:
     while p < n and lo[p] == hi[p]:
         p += 1
     return min(p, min(len(s) for s in seqs) - 1)
+
+
+def rotation_debias(pass_logits, pass_keys, question_passes, prior=None, temperature: float = 1.0):
+    """The ruling engine's log-space readout, in float64.
+
+    pass_logits[p]  the answer codes' logits of pass p (one per shown position)
+    pass_keys[p]    the option index each position of pass p shows
+    question_passes[q]  the passes of question q
+    prior           None, or a function K -> the K content-free log-probabilities by position
+    Per pass: log-softmax, minus the prior by position; per option: the mean of its values over
+    the question's passes; then softmax(raw / T).  Returns (raw list, probs list) per question.
+    """
+    raws, probs = [], []
+    for passes in question_passes:
+        K = len(pass_logits[passes[0]])
+        values = [[] for _ in range(K)]
+        for p in passes:
+            z = np.asarray(pass_logits[p], dtype=np.float64)
+            if z.shape[0] != K:
+                raise OracleError("passes of one question differ in size")
+            m = z.max()
+            lp = z - (m + np.log(np.exp(z - m).sum()))
+            if prior is not None:
+                lp = lp - np.asarray(prior(K), dtype=np.float64)
+            for pos, key in enumerate(pass_keys[p]):
+                values[int(key)].append(lp[pos])
+        raw = np.array([np.mean(v) for v in values])
+        t = raw / temperature
+        e = np.exp(t - t.max())
+        raws.append(raw)
+        probs.append(e / e.sum())
+    return raws, probs

@@ -55,6 +55,9 @@ _SIGNATURES = {
     "blink_shared_prefix_len_workspace": (_sz, []),
     "blink_shared_prefix_len": (_i32, [_vp, _i64, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "blink_kv_to_arena": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "blink_rotation_debias_workspace": (_sz, []),
+    "blink_rotation_debias": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp, _f32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     _vp, _sz, _vp]),
     "blink_label_readout_workspace": (_sz, [_i32]),
     "blink_label_readout": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
                                    _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -291,3 +294,29 @@ def blink_kv_to_arena(k_src, v_src, k_arena, v_arena, dst_slot: int, stream=None
                                  _ptr(k_arena), _ptr(v_arena), int(k_arena.stride(0)), int(k_arena.shape[0]),
                                  int(dst_slot), _stream(stream))
     _check(st, "blink_kv_to_arena")
+
+
+def blink_rotation_debias(logits, pass_off, key_of_pos, question_pass, raw_off, temperature: float, prior=None,
+                          raw=None, probs=None, host_probs=None, qtype=None, answers=None, host_answers=None,
+                          ws=None, stream=None):
+    """Per pass log-softmax minus the prior, the mean over each question's passes, then the
+    temperature softmax (and optional typed answers).  Returns (probs, raw, answers)."""
+    _need_cuda(logits, pass_off, key_of_pos, question_pass, raw_off, prior, raw, probs, qtype, answers)
+    n_pass = pass_off.numel() - 1
+    B = raw_off.numel() - 1
+    sum_k = int(raw_off[-1].item())
+    dev = logits.device
+    if probs is None:
+        probs = torch.empty(sum_k, dtype=torch.float32, device=dev)
+    if raw is None:
+        raw = torch.empty(sum_k, dtype=torch.float32, device=dev)
+    if qtype is not None and answers is None:
+        answers = torch.empty(B, 3, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = new_workspace(int(lib().blink_rotation_debias_workspace()), dev)
+    st = lib().blink_rotation_debias(_ptr(logits), _ptr(pass_off), _ptr(key_of_pos), int(n_pass), _ptr(question_pass),
+                                     _ptr(raw_off), int(B), sum_k, _ptr(prior), float(temperature), _ptr(raw),
+                                     _ptr(probs), _ptr(host_probs), _ptr(qtype), _ptr(answers), _ptr(host_answers),
+                                     _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "blink_rotation_debias")
+    return probs, raw, answers

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libblink.so")
-SOURCES = ["common.cu", "plan.cu", "readout.cu", "attention.cu", "prefix.cu"]
+SOURCES = ["common.cu", "plan.cu", "readout.cu", "attention.cu", "prefix.cu", "debias.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "answer.cuh"
 #include "common.cuh"
 
 namespace blink {
@@ -158,59 +159,7 @@ __global__ void __launch_bounds__(kReadoutWarps * 32)
         const int k = lo + lane + 32 * j;
         if (k < hi) probs[k] = v[j] * inv;
     }
-    if (qtype && answers) {
-        // blink.py `answer_for`: renormalise, then the question type's answer.
-        const int qt = __ldg(qtype + b);
-        float z = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) z += v[j] * inv;  // entries past the question are 0
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
-        const float rz = z > 0.f ? 1.0f / z : 1.0f;
-        float best = -1.f, ev = 0.f;
-        int best_k = 0x7FFFFFFF;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int kl = lane + 32 * j;  // label index inside the question
-            if (kl < K) {
-                const float pk = v[j] * inv * rz;
-                if (pk > best) {  // increasing kl: the first of equal values stays
-                    best = pk;
-                    best_k = kl;
-                }
-                ev = fmaf(static_cast<float>(kl), pk, ev);
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-            const int ok = __shfl_xor_sync(0xFFFFFFFFu, best_k, o);
-            if (ob > best || (ob == best && ok < best_k)) {
-                best = ob;
-                best_k = ok;
-            }
-            ev += __shfl_xor_sync(0xFFFFFFFFu, ev, o);
-        }
-        const float p_first = __shfl_sync(0xFFFFFFFFu, v[0] * inv * rz, 0);
-        if (lane == 0) {
-            const float inv_k = 1.0f / static_cast<float>(K);
-            const float conf = K > 1 ? (best - inv_k) / (1.0f - inv_k) : 1.0f;
-            float c = conf, val = best;
-            if (qt == 1) {  // noul: p of its first label ("yes"); no confidence
-                c = __int_as_float(0x7FC00000);
-                val = p_first;
-            } else if (qt == 2) {  // score: expected level, confidence clamped to [0, 1]
-                c = fminf(1.0f, fmaxf(0.0f, conf));
-                val = ev;
-            } else if (qt != 0) {
-                atomicCAS(err, 0, BLINK_DEVICE_FLAG);
-                c = val = __int_as_float(0x7FC00000);
-            }
-            answers[3 * b + 0] = static_cast<float>(best_k);
-            answers[3 * b + 1] = c;
-            answers[3 * b + 2] = val;
-        }
-    }
+    if (qtype && answers) write_answer(v, inv, K, lane, __ldg(qtype + b), answers + 3 * b, err);
 }
 
 }  // namespace
