@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle sample")
+    ap.add_argument("--no-rows", action="store_true", help="skip the measurements of the other path rows")
     ap.add_argument("--only", choices=["readout_stress"], default=None,
                     help="run one sub-measurement alone (for profiling) and print its JSON")
     return ap.parse_args()
@@ -358,6 +359,10 @@ def main():
     if not args.no_stress and rank == 0:
         line["roofline_readout_stress"] = readout_stress(blink, dev, hbm_peak, peak_kind, flush, args)
 
+    # ---- the other rows of the path, each timed alone (CUDA events, L2 flushed before each launch)
+    if not args.no_rows and rank == 0:
+        line["rows"] = other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind)
+
     # ---- end to end through the C ABI with host buffers (copies inside the timed region)
     if not args.no_e2e:
         line["e2e"] = e2e(blink, dev, w, lengths, ins, rd, flush, args, world)
@@ -368,6 +373,116 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def _time(fn, flush, reps=10):
+    """Mean device time (ms) of fn() over reps launches, L2 flushed before each."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = []
+    for _ in range(reps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
+    """The prefix side, several requests per launch and the log-space readout, on inputs shaped
+    like the long-document workload (synthetic, drawn on the device: timing only; parity is in
+    the tests)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    bf = torch.bfloat16
+    out = {}
+    P, Hq, Hkv, d = w.P, w.Hq, w.Hkv, w.d
+    # 1. the prefix's own causal self-attention: one sequence of P tokens, no prefix
+    q = torch.randn(P, Hq, d, generator=g, device=dev).to(bf)
+    k = torch.randn(P, Hkv, d, generator=g, device=dev).to(bf)
+    v = torch.randn(P, Hkv, d, generator=g, device=dev).to(bf)
+    cu1 = torch.tensor([0, P], dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    ws = blink.new_workspace(256, dev)
+    ms = _time(lambda: blink.blink_prefix_tail_attention(q, None, None, k, v, cu1, B=1, P=0, max_tail=P, out=o, ws=ws),
+               flush)
+    fl = attention_flops(np.array([P]), 0, Hq, d)
+    out["prefix_self_attention"] = {"ms": ms, "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / tc_peak,
+                                    "shape": f"one causal sequence of {P} tokens, {Hq}/{Hkv} heads, d {d}"}
+    # 2. the prefix K/V rows written into an arena region
+    slots = P + 4096
+    ak = torch.empty(slots, Hkv * d, dtype=bf, device=dev)
+    av = torch.empty_like(ak)
+    ms = _time(lambda: blink.blink_kv_to_arena(k, v, ak, av, 1024), flush)
+    nbytes = 2 * 2 * P * Hkv * d * 2
+    out["kv_to_arena"] = {"ms": ms, "GBs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_peak,
+                          "bytes": nbytes, "shape": f"{P} rows of K and V ({Hkv}x{d} bf16) read and written"}
+    del q, o
+    # 3. shared-prefix length over the questions' full prompts (prefix + tail each)
+    lengths = wl_tail_lengths(w)
+    pre = torch.randint(0, w.V, (P,), generator=g, device=dev, dtype=torch.int32)
+    seqs = [torch.cat([pre, torch.randint(0, w.V, (int(L),), generator=g, device=dev, dtype=torch.int32)])
+            for L in lengths]
+    toks = torch.cat(seqs)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum([P + int(L) for L in lengths])]), dtype=torch.int32, device=dev)
+    lout = torch.empty(1, dtype=torch.int32, device=dev)
+    lws = blink.new_workspace(256, dev)
+    ms = _time(lambda: blink.blink_shared_prefix_len(toks, cu, out=lout, sync=False, ws=lws), flush)
+    out["shared_prefix_len"] = {"ms": ms, "tokens": int(toks.numel()),
+                                "shape": f"{len(lengths)} prompts sharing {P} tokens"}
+    # 4. several requests in one launch: 8 requests, each a 2048-token prefix with 16 tails U[32,128]
+    rng = np.random.default_rng(21)
+    n_req, Pr = 8, 2048
+    tails = [rng.integers(32, 129, size=16) for _ in range(n_req)]
+    lens = np.concatenate(tails).astype(np.int32)
+    rows = int(lens.sum())
+    arena_k = torch.randn(n_req * Pr, Hkv, d, generator=g, device=dev).to(bf)
+    arena_v = torch.randn(n_req * Pr, Hkv, d, generator=g, device=dev).to(bf)
+    qm = torch.randn(rows, Hq, d, generator=g, device=dev).to(bf)
+    km = torch.randn(rows, Hkv, d, generator=g, device=dev).to(bf)
+    vm = torch.randn(rows, Hkv, d, generator=g, device=dev).to(bf)
+    cum = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+    req_rows = np.concatenate([[0], np.cumsum([t.sum() for t in tails])]).astype(np.int32)
+    om = torch.empty_like(qm)
+    mws = blink.new_workspace(256, dev)
+    ms = _time(lambda: blink.blink_prefix_tail_attention_multi(
+        qm, arena_k, arena_v, km, vm, cum, B=len(lens), req_rows=req_rows,
+        req_prefix_start=[r * Pr for r in range(n_req)], req_prefix_len=[Pr] * n_req, max_tail=128, out=om, ws=mws),
+        flush)
+    fl = sum(attention_flops(t, Pr, Hq, d) for t in tails)
+    out["several_requests"] = {"ms": ms, "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / tc_peak,
+                               "shape": f"{n_req} requests x (prefix {Pr}, 16 tails U[32,128]) in one launch"}
+    # 5. log-space readout over option orders: 512 questions x 4 orders x up to 26 options
+    B = 512
+    K = rng.integers(2, 27, size=B)
+    R = 4
+    pass_k = np.repeat(K, R)
+    pass_off = torch.tensor(np.concatenate([[0], np.cumsum(pass_k)]), dtype=torch.int32, device=dev)
+    keys = torch.tensor(np.concatenate([[(pos + r) % k for pos in range(k)] for k in K for r in range(R)]),
+                        dtype=torch.int32, device=dev)
+    logits = torch.randn(int(pass_k.sum()), generator=g, device=dev)
+    qpass = torch.arange(0, B * R + 1, R, dtype=torch.int32, device=dev)
+    raw_off = torch.tensor(np.concatenate([[0], np.cumsum(K)]), dtype=torch.int32, device=dev)
+    prior = torch.randn(255 * 255, generator=g, device=dev)
+    pr = torch.empty(int(K.sum()), dtype=torch.float32, device=dev)
+    rw = torch.empty_like(pr)
+    dws = blink.new_workspace(256, dev)
+    sk = int(K.sum())
+    ms = _time(lambda: blink.blink_rotation_debias(logits, pass_off, keys, qpass, raw_off, 1.0, prior=prior, raw=rw,
+                                                   probs=pr, ws=dws, sum_k=sk), flush)
+    out["rotation_debias"] = {"ms": ms, "shape": f"{B} questions x {R} orders x 2-26 options"}
+    return out
+
+
+def wl_tail_lengths(w):
+    from shared_prefix_question_gb300 import workloads as wl
+    return wl.tail_lengths(w)
 
 
 def readout_stress(blink, dev, hbm_peak, peak_kind, flush, args):

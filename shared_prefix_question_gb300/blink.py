@@ -298,13 +298,14 @@ def blink_kv_to_arena(k_src, v_src, k_arena, v_arena, dst_slot: int, stream=None
 
 def blink_rotation_debias(logits, pass_off, key_of_pos, question_pass, raw_off, temperature: float, prior=None,
                           raw=None, probs=None, host_probs=None, qtype=None, answers=None, host_answers=None,
-                          ws=None, stream=None):
+                          ws=None, sum_k: int | None = None, stream=None):
     """Per pass log-softmax minus the prior, the mean over each question's passes, then the
     temperature softmax (and optional typed answers).  Returns (probs, raw, answers)."""
     _need_cuda(logits, pass_off, key_of_pos, question_pass, raw_off, prior, raw, probs, qtype, answers)
     n_pass = pass_off.numel() - 1
     B = raw_off.numel() - 1
-    sum_k = int(raw_off[-1].item())
+    if sum_k is None:
+        sum_k = int(raw_off[-1].item())  # one small copy; pass sum_k to avoid it
     dev = logits.device
     if probs is None:
         probs = torch.empty(sum_k, dtype=torch.float32, device=dev)

@@ -134,7 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int req_begin = a.req_row[req], req_end = a.req_row[req + 1];
     const int P = a.req_P[req], pre_start = a.req_pre[req];
     const int n_pre = (P + BN - 1) / BN;
-    const int t0 = req_begin + (static_cast<int>(blockIdx.x) - a.req_blk[req]) * 2 * a.tpt;
+    // Within a request the blocks run from the last row pair to the first: with a causal tail the
+    // late pairs have the most keys, and starting them first shortens the end of the launch.
+    const int t0 = req_begin + (a.req_blk[req + 1] - 1 - static_cast<int>(blockIdx.x)) * 2 * a.tpt;
 
     if (threadIdx.x == kProducerWarp * 32) {
         ptx::mbar_init(q_full, 1);
@@ -379,9 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb = kbeg + (i - n_pre) * BN;
                 const int lo_j = q_lo - kb;
                 const int hi_j = owned ? tok - kb : -1;
+                // tiles every row of the warp sees whole (most of a long causal tail) need no mask
+                if (!__all_sync(0xFFFFFFFFu, lo_j <= 0 && hi_j >= BN - 1)) {
 #pragma unroll
-                for (int j = 0; j < BN; ++j)
-                    if (j < lo_j || j > hi_j) s[j] = -INFINITY;
+                    for (int j = 0; j < BN; ++j)
+                        if (j < lo_j || j > hi_j) s[j] = -INFINITY;
+                }
             }
             float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll

@@ -8,51 +8,49 @@
 namespace blink {
 namespace {
 
-constexpr int kLcpWarps = 8;
+constexpr int kLcpThreads = 256;
+constexpr int kLcpChunk = 1024;     // positions compared by one block per step (4 per thread)
+constexpr int kLcpBlocksPerSeq = 8;  // blocks sharing one sequence's chunks
 
-// One warp per sequence i >= 1: the first position where sequence i differs from sequence 0
-// (or the shorter length), folded into the global minimum; every sequence also folds len - 1,
-// so the result keeps at least one token of every sequence.  The common prefix of all sequences
-// is the minimum over i of the common prefix of sequences 0 and i.
-__global__ void __launch_bounds__(kLcpWarps * 32)
+// Block (x, i): sequence i against sequence 0, over chunks x, x + 8, ... of 1024 positions; the
+// first differing position (or the shorter length) is folded into the global minimum.  Each
+// sequence's block 0 also folds len - 1, so every sequence keeps at least one token.  The common
+// prefix of all sequences is the minimum over i of the common prefix of sequences 0 and i.
+__global__ void __launch_bounds__(kLcpThreads)
     lcp_kernel(const int32_t *__restrict__ tokens, int64_t n_tokens, const int32_t *__restrict__ cu, int n,
                int *__restrict__ out, int *__restrict__ err)
 {
-    const int lane = threadIdx.x & 31;
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int warps = (gridDim.x * blockDim.x) >> 5;
+    __shared__ int s_first;
+    const int i = blockIdx.y;
     const int base0 = __ldg(cu);  // token offsets are relative to cu[0]
     const int len0 = __ldg(cu + 1) - base0;
-    if (len0 < 1 || len0 > n_tokens) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) atomicCAS(err, 0, BLINK_DEVICE_FLAG);
+    const int bi = __ldg(cu + i) - base0;
+    const int len = __ldg(cu + i + 1) - __ldg(cu + i);
+    if (len0 < 1 || static_cast<int64_t>(len0) > n_tokens || len < 1 || bi < 0 ||
+        static_cast<int64_t>(bi) + len > n_tokens) {
+        if (threadIdx.x == 0) atomicCAS(err, 0, BLINK_DEVICE_FLAG);
         return;
     }
-    for (int i = warp; i < n; i += warps) {
-        const int bi = __ldg(cu + i) - base0;
-        const int len = __ldg(cu + i + 1) - __ldg(cu + i);
-        if (len < 1 || bi < 0 || static_cast<int64_t>(bi) + len > n_tokens) {
-            if (lane == 0) atomicCAS(err, 0, BLINK_DEVICE_FLAG);
-            continue;
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicMin(out, len - 1);
+    if (i == 0) return;
+    const int lim = min(len0, len);
+    for (int c0 = blockIdx.x * kLcpChunk; c0 < lim; c0 += gridDim.x * kLcpChunk) {
+        if (threadIdx.x == 0) s_first = *reinterpret_cast<volatile int *>(out);
+        __syncthreads();
+        const int known = s_first;  // a mismatch at or past the current minimum changes nothing
+        __syncthreads();
+        if (c0 >= known) break;
+        int first = INT_MAX;
+#pragma unroll
+        for (int u = 0; u < kLcpChunk / kLcpThreads; ++u) {
+            const int j = c0 + u * kLcpThreads + threadIdx.x;
+            if (j < lim && first == INT_MAX && __ldg(tokens + j) != __ldg(tokens + bi + j)) first = j;
         }
-        if (lane == 0) atomicMin(out, len - 1);
-        if (i == 0) continue;
-        const int lim = min(len0, len);
-        int p = lim;
-        for (int j0 = 0; j0 < lim; j0 += 32) {
-            if (j0 >= *reinterpret_cast<volatile int *>(out)) {  // cannot lower the minimum any more
-                p = j0;
-                break;
-            }
-            const int j = j0 + lane;
-            const bool diff = j < lim && __ldg(tokens + j) != __ldg(tokens + bi + j);
-            const unsigned m = __ballot_sync(0xFFFFFFFFu, diff);
-            if (m) {
-                p = j0 + __ffs(m) - 1;
-                break;
-            }
-        }
-        if (lane == 0) atomicMin(out, p);
+        if (first != INT_MAX) atomicMin(out, first);
+        if (__syncthreads_or(first != INT_MAX)) break;  // later chunks of this block cannot be smaller
     }
+    // No difference before lim: the common prefix of the pair is lim, which the len - 1 folds
+    // already undercut, so nothing more to fold.
 }
 
 // Copies n rows of `row_elems` bf16 values (16-byte chunks) from src (row stride src_stride) to
@@ -104,10 +102,8 @@ extern "C" blink_status blink_shared_prefix_len(const int32_t *d_tokens, int64_t
     } else {
         // 0x7F7F7F7F: larger than any length, the start of the minimum
         if (cudaMemsetAsync(d_len, 0x7F, sizeof(int32_t), stream) != cudaSuccess) return BLINK_CUDA_ERROR;
-        const int sms = sm_count_prefix();
-        int grid = (n + kLcpWarps - 1) / kLcpWarps;
-        if (sms > 0 && grid > 4 * sms) grid = 4 * sms;
-        lcp_kernel<<<grid, kLcpWarps * 32, 0, stream>>>(d_tokens, n_tokens, d_cu, n, d_len, &hdr->error);
+        dim3 grid(kLcpBlocksPerSeq, static_cast<unsigned>(n));
+        lcp_kernel<<<grid, kLcpThreads, 0, stream>>>(d_tokens, n_tokens, d_cu, n, d_len, &hdr->error);
         if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
     }
     if (h_len) {
