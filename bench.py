@@ -517,7 +517,9 @@ def readout_stress(blink, dev, hbm_peak, peak_kind, flush, args):
     achieved = nbytes / (ms / 1000.0) / 1e9
     del W
     return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-            "traffic": None, "kernel": "readout_kernel", "ms": ms, "algorithmic_bytes": nbytes,
+            "traffic": traffic_record(os.path.join(ROOT, "shared_prefix_question_gb300", "csrc", "readout.cu"),
+                                      "readout_stress"),
+            "kernel": "readout_kernel", "ms": ms, "algorithmic_bytes": nbytes,
             "input": f"512 questions, {len(ids)} labels ({distinct} distinct rows) drawn per question without "
                      f"replacement from {w.V}, hidden {w.H}; includes the counter memset",
             "peak_kind": f"{peak_kind} copy bandwidth"}

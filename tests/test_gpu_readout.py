@@ -139,3 +139,88 @@ def test_readout_answers(name):
             else:
                 assert abs(got[b, 1] - ref["confidence"]) <= 2e-3
             assert abs(got[b, 2] - ref["value"]) <= tol
+
+
+@pytest.mark.parametrize("with_slots", [False, True])
+def test_readout_rows_ordered_by_id_match_request_order(with_slots):
+    """Above 64 MiB of offered rows the readout first orders the labels so that those of one
+    vocabulary id run back to back (the repeats of a row then come from L2).  Each label's FP32
+    dot is the same sum in either order, so logits and probabilities equal, bit for bit, those
+    of the entry point that keeps request order, and they match the oracle.  Questions share a
+    pool of ids (blink.py `render` offers the first K labels of one pool) and some repeat an id
+    inside one question; H = 5128 leaves a ragged last batch of chunks."""
+    rng = np.random.default_rng(31 + with_slots)
+    H, V, B = 5128, 4000, 400
+    pool = rng.choice(V, 40, replace=False)
+    ks = rng.integers(1, 41, size=B)
+    parts = []
+    for b, k in enumerate(ks):
+        if b % 7 == 0:
+            parts.append(rng.choice(V, k))  # repeats inside one question too
+        elif b % 2:
+            parts.append(pool[:k])
+        else:
+            parts.append(rng.permutation(pool)[:k])
+    off = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    ids = np.concatenate(parts).astype(np.int32)
+    assert len(ids) * H * 2 > 64 << 20  # the ordered path
+    rows = B + 5
+    hidden = wl.normal_bf16(rng, (rows, H))
+    W = wl.normal_bf16(rng, (V, H), std=0.02)
+    last = rng.permutation(rows)[:B].astype(np.int32)
+    slot_of = rng.permutation(B).astype(np.int32) if with_slots else None
+    per_slot = np.empty(B, dtype=np.int32)
+    if with_slots:
+        per_slot[slot_of] = last  # question b reads last_by_slot[slot_of[b]] == last[b]
+    ins = wl.ReadoutInputs(hidden, last, W, off, ids, 0.7)
+    d_hidden, d_W, d_off, d_ids = dev_bf16(hidden), dev_bf16(W), dev_i32(off), dev_i32(ids)
+    d_last = dev_i32(per_slot if with_slots else last)
+    d_slot = dev_i32(slot_of) if with_slots else None
+    lg_ordered = torch.empty(len(ids), dtype=torch.float32, device="cuda")
+    lg_request = torch.empty_like(lg_ordered)
+    p_ordered, ws = blink.blink_label_readout(d_hidden, d_last, d_W, d_off, d_ids, 0.7, logits=lg_ordered,
+                                              slot_of=d_slot)
+    p_request = blink.blink_label_readout_noalloc(d_hidden, d_last, d_W, d_off, d_ids, 0.7, logits=lg_request,
+                                                  slot_of=d_slot)
+    torch.cuda.synchronize()
+    assert blink.blink_read_device_status(ws) == blink.BLINK_OK
+    assert torch.equal(lg_ordered, lg_request)
+    assert torch.equal(p_ordered, p_request)
+    compare_readout(p_ordered.cpu().numpy().astype(np.float64), ins)
+
+
+@pytest.mark.parametrize("with_slots", [False, True])
+def test_readout_ragged_rows_and_shared_ids(with_slots):
+    """Full-size rows whose last batch of 16-byte chunks is ragged (H = 5128: two batches of 256
+    chunks, then 129), label ids shared across questions (blink.py `render` offers the first K
+    labels of one pool) and repeated inside some questions, hidden rows reached through a slot
+    map: the probabilities match the oracle."""
+    rng = np.random.default_rng(31 + with_slots)
+    H, V, B = 5128, 4000, 120
+    pool = rng.choice(V, 40, replace=False)
+    ks = rng.integers(1, 41, size=B)
+    parts = []
+    for b, k in enumerate(ks):
+        if b % 7 == 0:
+            parts.append(rng.choice(V, k))  # repeats inside one question too
+        elif b % 2:
+            parts.append(pool[:k])
+        else:
+            parts.append(rng.permutation(pool)[:k])
+    off = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    ids = np.concatenate(parts).astype(np.int32)
+    rows = B + 5
+    hidden = wl.normal_bf16(rng, (rows, H))
+    W = wl.normal_bf16(rng, (V, H), std=0.02)
+    last = rng.permutation(rows)[:B].astype(np.int32)
+    slot_of = rng.permutation(B).astype(np.int32) if with_slots else None
+    per_slot = np.empty(B, dtype=np.int32)
+    if with_slots:
+        per_slot[slot_of] = last  # question b reads last_by_slot[slot_of[b]] == last[b]
+    ins = wl.ReadoutInputs(hidden, last, W, off, ids, 0.7)
+    probs, ws = blink.blink_label_readout(dev_bf16(hidden), dev_i32(per_slot if with_slots else last), dev_bf16(W),
+                                          dev_i32(off), dev_i32(ids), 0.7,
+                                          slot_of=dev_i32(slot_of) if with_slots else None)
+    torch.cuda.synchronize()
+    assert blink.blink_read_device_status(ws) == blink.BLINK_OK
+    compare_readout(probs.cpu().numpy().astype(np.float64), ins)
