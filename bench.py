@@ -351,8 +351,10 @@ def main():
                        "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB written then read back)",
                        "parallelism": f"replicas x{world}, questions sharded, no collective in the step"},
             "prefill_tokens_per_s": world * prefill_tokens / (ms_per_step / 1000.0),
+            "tail_tokens_per_s": world * int(lengths.sum()) / (ms_per_step / 1000.0),
             "kernels_ms": {"plan": statistics.mean(plan_ms), "attention": attn_mean,
                            "readout": statistics.mean(read_ms)},
+            "spread_ms": {"step": spread(step_ms), "attention": spread(attn_ms)},
             "roofline": roofline, "gpu_launches": 3 * args.steps, "clocks": clocks}
 
     # ---- readout on the stress input (HBM-bound at scale)
@@ -375,8 +377,8 @@ def main():
         dist.destroy_process_group()
 
 
-def _time(fn, flush, reps=10):
-    """Mean device time (ms) of fn() over reps launches, L2 flushed before each."""
+def _time_all(fn, flush, reps=10):
+    """Device times (ms) of fn() over reps launches, L2 flushed before each."""
     import torch
     fn()
     torch.cuda.synchronize()
@@ -390,7 +392,50 @@ def _time(fn, flush, reps=10):
         e1.record(stream)
         evs.append((e0, e1))
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def _time(fn, flush, reps=10):
+    """Mean device time (ms) of fn() over reps launches, L2 flushed before each."""
+    return statistics.mean(_time_all(fn, flush, reps))
+
+
+def spread(ms):
+    """Median and 10th / 90th percentiles of a list of times."""
+    q = np.percentile(np.asarray(ms, dtype=np.float64), [10, 50, 90])
+    return {"p10": float(q[0]), "median": float(q[1]), "p90": float(q[2])}
+
+
+def attention_config_row(blink, dev, name, tc_peak, hbm_peak, flush):
+    """The prefix-tail attention on one of the other workloads (lengths and shapes from the
+    workload table, values drawn on the device): FLOP fraction, and for the plain causal
+    workload, which sits near the ridge, the byte fraction too (Q, K, V read and O written once)."""
+    import torch
+    from shared_prefix_question_gb300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    lengths = wl.tail_lengths(w).astype(np.int32)
+    rows = int(lengths.sum())
+    g = torch.Generator(device=dev)
+    g.manual_seed(100 + w.index)
+    bf = torch.bfloat16
+    q = torch.randn(rows, w.Hq, w.d, generator=g, device=dev).to(bf)
+    kt = torch.randn(rows, w.Hkv, w.d, generator=g, device=dev).to(bf)
+    vt = torch.randn(rows, w.Hkv, w.d, generator=g, device=dev).to(bf)
+    kp = torch.randn(w.P, w.Hkv, w.d, generator=g, device=dev).to(bf) if w.P else None
+    vp = torch.randn(w.P, w.Hkv, w.d, generator=g, device=dev).to(bf) if w.P else None
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    ws = blink.new_workspace(blink.attention_workspace_bytes(rows, len(lengths), w.P, w.Hq, w.Hkv, w.d), dev)
+    ms_all = _time_all(lambda: blink.blink_prefix_tail_attention(q, kp, vp, kt, vt, cu, B=len(lengths), P=w.P,
+                                                                 max_tail=int(lengths.max()), out=o, ws=ws), flush)
+    ms = statistics.mean(ms_all)
+    fl = attention_flops(lengths, w.P, w.Hq, w.d)
+    row = {"ms": ms, **spread(ms_all), "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / tc_peak,
+           "shape": w.description}
+    if not w.P:
+        nbytes = rows * (2 * w.Hq + 2 * w.Hkv) * w.d * 2
+        row.update({"bytes": nbytes, "GBs": nbytes / ms / 1e6, "byte_frac": nbytes / ms / 1e6 / hbm_peak})
+    return row
 
 
 def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
@@ -402,6 +447,9 @@ def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
     g.manual_seed(11)
     bf = torch.bfloat16
     out = {}
+    # 0. the attention on the other workloads of the table (the 18k one is the step above)
+    for name in ("2k", "plain", "max"):
+        out[f"attention_{name}"] = attention_config_row(blink, dev, name, tc_peak, hbm_peak, flush)
     P, Hq, Hkv, d = w.P, w.Hq, w.Hkv, w.d
     # 1. the prefix's own causal self-attention: one sequence of P tokens, no prefix
     q = torch.randn(P, Hq, d, generator=g, device=dev).to(bf)

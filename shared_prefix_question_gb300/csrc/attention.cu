@@ -97,6 +97,34 @@ __device__ __forceinline__ int owner_floor(const AttnArgs &a, int t)
     return ans;
 }
 
+// The same search by a whole warp (every lane gets the answer): 32 probes per round, so 2-3
+// dependent rounds of loads instead of one per halving.  Starts ascend with b.
+__device__ __forceinline__ int owner_floor_warp(const AttnArgs &a, int t, int lane)
+{
+    int lo = 0, n = a.B;  // candidates [lo, lo + n); start_lo <= t once past the first round
+    while (n > 32) {
+        const int step = (n + 31) / 32;
+        const int idx = lo + lane * step;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, idx < lo + n && start_of(a, idx) <= t);
+        if (m == 0) return -1;  // the first start is past t
+        const int nlo = lo + (31 - __clz(m)) * step;
+        n = min(step, lo + n - nlo);
+        lo = nlo;
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, lane < n && start_of(a, lo + lane) <= t);
+    return m ? lo + 31 - __clz(m) : -1;
+}
+
+// Largest b >= b0 with start_b <= t, walking forward from b0 (start_b0 <= t, or b0 = -1); after
+// eight steps (many short questions inside one block) it falls back to the binary search.
+__device__ __forceinline__ int owner_from(const AttnArgs &a, int t, int b0)
+{
+    int b = b0;
+    for (int steps = 0; b + 1 < a.B && start_of(a, b + 1) <= t; ++b)
+        if (++steps > 8) return owner_floor(a, t);
+    return b;
+}
+
 __device__ __forceinline__ bool question_ok(const AttnArgs &a, int s, int L)
 {
     return L >= 1 && L <= a.max_tail && s >= 0 && static_cast<long long>(s) + L <= a.rows;
@@ -123,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *o_full = bars + 13;  // [2]
     uint64_t *mma_done = bars + 15;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 16);
-    int *sched = reinterpret_cast<int *>(tmem_holder + 1);  // kbeg, n_tail, abort
+    int *sched = reinterpret_cast<int *>(tmem_holder + 1);  // kbeg, n_tail, abort, first owner
     volatile int *abort_flag = sched + 2;
 
     const int warp = threadIdx.x >> 5;
@@ -138,27 +166,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     // late pairs have the most keys, and starting them first shortens the end of the launch.
     const int t0 = req_begin + (a.req_blk[req + 1] - 1 - static_cast<int>(blockIdx.x)) * 2 * a.tpt;
 
-    if (threadIdx.x == kProducerWarp * 32) {
-        ptx::mbar_init(q_full, 1);
-        for (int i = 0; i < kSlots; ++i) {
-            ptx::mbar_init(full + i, 1);
-            ptx::mbar_init(empty + i, 1);
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            ptx::mbar_init(q_full, 1);
+            for (int i = 0; i < kSlots; ++i) {
+                ptx::mbar_init(full + i, 1);
+                ptx::mbar_init(empty + i, 1);
+            }
+            for (int t = 0; t < 2; ++t) {
+                ptx::mbar_init(s_full + t, 1);
+                ptx::mbar_init(p_full + t, 128);
+                ptx::mbar_init(o_full + t, 1);
+            }
+            ptx::mbar_init(mma_done, 1);
+            ptx::fence_mbar_init();
+            sched[2] = 0;
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_kpre);
+            ptx::tma_prefetch_desc(&tm_vpre);
+            ptx::tma_prefetch_desc(&tm_ktail);
+            ptx::tma_prefetch_desc(&tm_vtail);
+            // The Q tiles need no schedule: request them first.  The second tile is loaded only
+            // if it starts inside the request (its rows past the tensor's end are then
+            // zero-filled by the copy); otherwise its rows stay as they are and are never stored.
+            // (Rows past g * tpt, zeroed below by the other warps, are outside the copied box.)
+            const uint32_t q_box = 64u * a.g * a.tpt * 2u;
+            const int q_tiles = (t0 + a.tpt < req_end) ? 2 : 1;
+            ptx::mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(q_tiles) * L::kPanels * q_box);
+            for (int t = 0; t < q_tiles; ++t)
+                for (int p = 0; p < L::kPanels; ++p)
+                    ptx::tma_load_3d((t == 0 ? q_s0 : q_s1) + p * kHalfBytes, &tm_q, p * 64, head * a.g,
+                                     t0 + t * a.tpt, q_full);
         }
-        for (int t = 0; t < 2; ++t) {
-            ptx::mbar_init(s_full + t, 1);
-            ptx::mbar_init(p_full + t, 128);
-            ptx::mbar_init(o_full + t, 1);
-        }
-        ptx::mbar_init(mma_done, 1);
-        ptx::fence_mbar_init();
+        __syncwarp();
         // Tail keys this block needs: from the start of the first question it touches.
         const int t_end = min(t0 + 2 * a.tpt, req_end);
         int kbeg = -1;
-        int b = owner_floor(a, t0);
+        const int b = owner_floor_warp(a, t0, lane);
         if (b >= 0) {
             const int s = start_of(a, b), len = len_of(a, b);
-            if (!question_ok(a, s, len) || (t0 < s + len && s < req_begin)) atomicCAS(a.err, 0, BLINK_DEVICE_FLAG);
-            else if (t0 < s + len) kbeg = s;
+            if (!question_ok(a, s, len) || (t0 < s + len && s < req_begin)) {
+                if (lane == 0) atomicCAS(a.err, 0, BLINK_DEVICE_FLAG);
+            } else if (t0 < s + len) {
+                kbeg = s;
+            }
         }
         if (kbeg < 0 && b + 1 < a.B) {
             const int s = start_of(a, b + 1);
@@ -166,14 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int n_tail = 0;
         if (kbeg >= 0 && kbeg < t_end) n_tail = (t_end - kbeg + BN - 1) / BN;
-        sched[0] = kbeg < 0 ? 0 : kbeg;
-        sched[1] = n_tail;
-        sched[2] = 0;
-        ptx::tma_prefetch_desc(&tm_q);
-        ptx::tma_prefetch_desc(&tm_kpre);
-        ptx::tma_prefetch_desc(&tm_vpre);
-        ptx::tma_prefetch_desc(&tm_ktail);
-        ptx::tma_prefetch_desc(&tm_vtail);
+        if (lane == 0) {
+            sched[0] = kbeg < 0 ? 0 : kbeg;
+            sched[1] = n_tail;
+            sched[3] = b;  // owner of the block's first token, where the softmax rows' searches start
+        }
     }
     if (warp == 0) {
         ptx::tmem_alloc(tmem_holder, kTmemCols);
@@ -204,17 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            const uint32_t q_box = 64u * a.g * a.tpt * 2u;
-            // The second tile is loaded only if it starts inside the tensor (its rows past the end
-            // are then zero-filled by the copy); otherwise its rows stay as they are and are never
-            // stored.
-            const int q_tiles = (t0 + a.tpt < req_end) ? 2 : 1;
             int n = 0;
-            ptx::mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(q_tiles) * L::kPanels * q_box);
-            for (int t = 0; t < q_tiles; ++t)
-                for (int p = 0; p < L::kPanels; ++p)
-                    ptx::tma_load_3d((t == 0 ? q_s0 : q_s1) + p * kHalfBytes, &tm_q, p * 64, head * a.g,
-                                     t0 + t * a.tpt, q_full);
             for (int it = 0; it < n_iter; ++it) {
                 const bool pre = it < n_pre;
                 const int kb = pre ? pre_start + it * BN : kbeg + (it - n_pre) * BN;
@@ -341,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool owned = false;
         int q_lo = 0;
         if (row_ok) {
-            const int b = owner_floor(a, tok);
+            const int b = owner_from(a, tok, sched[3]);
             if (b >= 0) {
                 const int s = start_of(a, b), len = len_of(a, b);
                 if (!question_ok(a, s, len) || (tok < s + len && s < req_begin)) {
