@@ -183,9 +183,22 @@ def cpu_baseline(w, lengths, ins, rd, target_s: float, n_threads: int = 0):
         tq = run(q)
     else:
         tq = t1
+    # one core: the first 16 tail tokens of question 0 (every head), scaled to whole questions
+    n_tok = int(min(16, ins.seq_len[0]))
+    toks = np.arange(ins.seq_start[0], ins.seq_start[0] + n_tok)
+    t0 = time.perf_counter()
+    oracle.prefix_tail_attention(ins.q, ins.k_pre, ins.v_pre, ins.k_tail, ins.v_tail, ins.seq_start, ins.seq_len,
+                                 ins.P, ins.Hq, ins.Hkv, ins.d,
+                                 select=(np.repeat(toks, ins.Hq).astype(np.int32),
+                                         np.tile(np.arange(ins.Hq), n_tok).astype(np.int32)), n_threads=1)
+    t_one = time.perf_counter() - t0
+    per_question = t_one / n_tok * float(np.mean(ins.seq_len))
     return {"value": q / tq, "unit": "questions/s", "cores": cores, "kind": "oracle",
             "sample": f"{q} of {w.n} questions (all heads and tail rows; plan over all {w.n}), "
-                      f"{tq:.1f} s of FP64 CPU work"}, q, tq
+                      f"{tq:.1f} s of FP64 CPU work",
+            "single_core": {"value": 1.0 / per_question, "unit": "questions/s",
+                            "sample": f"attention of {n_tok} tail tokens x {ins.Hq} heads of question 0 on one "
+                                      f"core ({t_one:.1f} s), scaled to the mean tail length"}}, q, tq
 
 
 def run_reference(args):
@@ -506,7 +519,13 @@ def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
     fl = sum(attention_flops(t, Pr, Hq, d) for t in tails)
     out["several_requests"] = {"ms": ms, "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / tc_peak,
                                "shape": f"{n_req} requests x (prefix {Pr}, 16 tails U[32,128]) in one launch"}
-    # 5. log-space readout over option orders: 512 questions x 4 orders x up to 26 options
+    # 5. the pack plan at its largest size: 64 requests x 512 questions (32768 lengths U[16,1024])
+    plan_len = torch.randint(16, 1025, (32768,), generator=g, device=dev, dtype=torch.int32)
+    pout = None
+    pout = blink.blink_pack_plan(plan_len, 32768, 0, out=pout)
+    ms = _time(lambda: blink.blink_pack_plan(plan_len, 32768, 0, out=pout, sync=False), flush)
+    out["pack_plan_32768"] = {"ms": ms, "shape": "32768 lengths U[16,1024], budget 32768 (64 requests x 512)"}
+    # 6. log-space readout over option orders: 512 questions x 4 orders x up to 26 options
     B = 512
     K = rng.integers(2, 27, size=B)
     R = 4
