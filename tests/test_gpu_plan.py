@@ -24,7 +24,9 @@ def _check(lengths, budget, max_rows):
     np.testing.assert_array_equal(d["slot_of"].cpu().numpy(), inv)
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 64, 255, 256, 1000, 4096, 32768])
+# 2049 and up: the keys are sorted over the whole GPU (block-sorted runs of 1024, then merge
+# rounds), including a short last run (2049, 5000, 17000) and an unpaired one (9000)
+@pytest.mark.parametrize("n", [1, 2, 3, 64, 255, 256, 1000, 2048, 2049, 4096, 5000, 9000, 17000, 32768])
 def test_plan_random(n):
     rng = np.random.default_rng(n)
     for budget, max_rows, hi in ((32768, 0, 1000), (32768, 7, 256), (100, 0, 60), (1, 0, 5), (10 ** 9, 0, 131072),
@@ -56,6 +58,11 @@ def test_plan_rejects_bad_length_on_device():
         lengths = np.array([5, bad, 7], dtype=np.int32)
         with pytest.raises(blink.BlinkError) as e:
             blink.blink_pack_plan(dev_i32(lengths), 100, 0, sync=True)
+        assert e.value.status == blink.BLINK_DEVICE_FLAG
+        big = np.full(6000, 9, dtype=np.int32)  # the whole-GPU sort path flags it the same way
+        big[4321] = bad
+        with pytest.raises(blink.BlinkError) as e:
+            blink.blink_pack_plan(dev_i32(big), 100, 0, sync=True)
         assert e.value.status == blink.BLINK_DEVICE_FLAG
     d = blink.blink_pack_plan(dev_i32(np.array([5, 7], dtype=np.int32)), 100, 0, sync=False)
     torch.cuda.synchronize()
