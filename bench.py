@@ -419,14 +419,15 @@ def spread(ms):
     return {"p10": float(q[0]), "median": float(q[1]), "p90": float(q[2])}
 
 
-def attention_config_row(blink, dev, name, tc_peak, hbm_peak, flush):
+def attention_config_row(blink, dev, name, tc_peak, hbm_peak, flush, lengths=None, header_only_ws=False):
     """The prefix-tail attention on one of the other workloads (lengths and shapes from the
     workload table, values drawn on the device): FLOP fraction, and for the plain causal
     workload, which sits near the ridge, the byte fraction too (Q, K, V read and O written once)."""
     import torch
     from shared_prefix_question_gb300 import workloads as wl
     w = wl.WORKLOADS[name]
-    lengths = wl.tail_lengths(w).astype(np.int32)
+    if lengths is None:
+        lengths = wl.tail_lengths(w).astype(np.int32)
     rows = int(lengths.sum())
     g = torch.Generator(device=dev)
     g.manual_seed(100 + w.index)
@@ -438,13 +439,16 @@ def attention_config_row(blink, dev, name, tc_peak, hbm_peak, flush):
     vp = torch.randn(w.P, w.Hkv, w.d, generator=g, device=dev).to(bf) if w.P else None
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device=dev)
     o = torch.empty_like(q)
-    ws = blink.new_workspace(blink.attention_workspace_bytes(rows, len(lengths), w.P, w.Hq, w.Hkv, w.d), dev)
+    # a header-only workspace leaves no room for prefix chunks: the unsplit kernel, for comparison
+    ws = blink.new_workspace(256 if header_only_ws else
+                             blink.attention_workspace_bytes(rows, len(lengths), w.P, w.Hq, w.Hkv, w.d), dev)
     ms_all = _time_all(lambda: blink.blink_prefix_tail_attention(q, kp, vp, kt, vt, cu, B=len(lengths), P=w.P,
                                                                  max_tail=int(lengths.max()), out=o, ws=ws), flush)
     ms = statistics.mean(ms_all)
     fl = attention_flops(lengths, w.P, w.Hq, w.d)
     row = {"ms": ms, **spread(ms_all), "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / tc_peak,
-           "shape": w.description}
+           "shape": w.description if len(lengths) == w.n else f"{len(lengths)} question(s), tails {list(lengths)}, "
+                                                                 f"prefix {w.P}, {w.Hq}/{w.Hkv} heads"}
     if not w.P:
         nbytes = rows * (2 * w.Hq + 2 * w.Hkv) * w.d * 2
         row.update({"bytes": nbytes, "GBs": nbytes / ms / 1e6, "byte_frac": nbytes / ms / 1e6 / hbm_peak})
@@ -460,9 +464,14 @@ def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
     g.manual_seed(11)
     bf = torch.bfloat16
     out = {}
-    # 0. the attention on the other workloads of the table (the 18k one is the step above)
+    # 0. the attention on the other workloads of the table (the 18k one is the step above), and
+    # one question against the 18k prefix (a small grid: the prefix is split into chunks)
     for name in ("2k", "plain", "max"):
         out[f"attention_{name}"] = attention_config_row(blink, dev, name, tc_peak, hbm_peak, flush)
+    out["attention_one_question_18k"] = attention_config_row(blink, dev, "18k", tc_peak, hbm_peak, flush,
+                                                             lengths=np.array([128], dtype=np.int32))
+    out["attention_one_question_18k_unsplit"] = attention_config_row(
+        blink, dev, "18k", tc_peak, hbm_peak, flush, lengths=np.array([128], dtype=np.int32), header_only_ws=True)
     P, Hq, Hkv, d = w.P, w.Hq, w.Hkv, w.d
     # 1. the prefix's own causal self-attention: one sequence of P tokens, no prefix
     q = torch.randn(P, Hq, d, generator=g, device=dev).to(bf)

@@ -55,6 +55,13 @@ struct AttnArgs {
     // Requests: request r owns tail rows [req_row[r], req_row[r+1]) and the prefix of req_P[r]
     // tokens at arena slots [req_pre[r], req_pre[r] + req_P[r]).  Blocks [req_blk[r], req_blk[r+1])
     // work on request r (a block never straddles two requests).
+    // Split of the prefix (one request only): with n_split > 1 the prefix tiles are cut into
+    // chunks of split_tiles; unit (row pair, kv head, chunk) writes its partial O (normalised by
+    // its own sum) and LSE, the last chunk also runs the tail tiles, and split_merge_kernel then
+    // merges the chunks of every row by LSE.
+    int n_split, split_tiles;
+    float *part_o;    // [units][n_split][2 BM][D], unit = row pair * Hkv + kv head
+    float *part_lse;  // [units][n_split][2 BM]
     int n_req;
     int req_row[kMaxRequests + 1];
     int req_blk[kMaxRequests + 1];
@@ -130,7 +137,9 @@ __device__ __forceinline__ bool question_ok(const AttnArgs &a, int s, int L)
     return L >= 1 && L <= a.max_tail && s >= 0 && static_cast<long long>(s) + L <= a.rows;
 }
 
-template <int D>
+// kSplit: this launch runs prefix chunks (n_split > 1) and writes partial results; without it
+// the chunk arithmetic folds away and the kernel is the plain one.
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kpre,
                      const __grid_constant__ CUtensorMap tm_vpre, const __grid_constant__ CUtensorMap tm_ktail,
@@ -157,14 +166,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int head = blockIdx.y;
+    const int split = kSplit ? static_cast<int>(blockIdx.x) % a.n_split : 0;  // prefix chunk
+    const int bx = kSplit ? static_cast<int>(blockIdx.x) / a.n_split : static_cast<int>(blockIdx.x);  // row pair
     int req = 0;  // this block's request
-    while (req + 1 < a.n_req && a.req_blk[req + 1] <= static_cast<int>(blockIdx.x)) ++req;
+    while (req + 1 < a.n_req && a.req_blk[req + 1] <= bx) ++req;
     const int req_begin = a.req_row[req], req_end = a.req_row[req + 1];
     const int P = a.req_P[req], pre_start = a.req_pre[req];
-    const int n_pre = (P + BN - 1) / BN;
+    const int pre_lo = kSplit ? split * a.split_tiles : 0;  // first prefix tile of this unit
+    const int n_pre = kSplit ? max(0, min((P + BN - 1) / BN - pre_lo, a.split_tiles)) : (P + BN - 1) / BN;
+    const bool has_tail = !kSplit || split == a.n_split - 1;
     // Within a request the blocks run from the last row pair to the first: with a causal tail the
     // late pairs have the most keys, and starting them first shortens the end of the launch.
-    const int t0 = req_begin + (a.req_blk[req + 1] - 1 - static_cast<int>(blockIdx.x)) * 2 * a.tpt;
+    const int t0 = req_begin + (a.req_blk[req + 1] - 1 - bx) * 2 * a.tpt;
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -219,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kbeg >= 0 && kbeg < t_end) n_tail = (t_end - kbeg + BN - 1) / BN;
         if (lane == 0) {
             sched[0] = kbeg < 0 ? 0 : kbeg;
-            sched[1] = n_tail;
+            sched[1] = has_tail ? n_tail : 0;
             sched[3] = b;  // owner of the block's first token, where the softmax rows' searches start
         }
     }
@@ -255,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int n = 0;
             for (int it = 0; it < n_iter; ++it) {
                 const bool pre = it < n_pre;
-                const int kb = pre ? pre_start + it * BN : kbeg + (it - n_pre) * BN;
+                const int kb = pre ? pre_start + (pre_lo + it) * BN : kbeg + (it - n_pre) * BN;
                 bool ok = true;
                 for (int kv = 0; kv < 2; ++kv) {
                     const int slot = n % kSlots;
@@ -408,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // masks
             if (i < n_pre) {
-                const int kb = i * BN;
+                const int kb = (pre_lo + i) * BN;
                 if (kb + BN > P) {
                     const int lim = P - kb;
 #pragma unroll
@@ -476,10 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_before();
             ptx::mbar_arrive(p_full + t);
         }
-        // epilogue: O / l -> bf16
+        // epilogue: O / l -> bf16 (or, for a prefix chunk, the partial O / l in fp32 and its LSE)
         if (ok && ptx::mbar_wait(o_full + t, 0, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)) {
             ptx::tc_fence_after();
             const float inv = (owned && l > 0.f) ? 1.0f / l : 0.f;
+            const float row_lse =
+                (owned && l > 0.f) ? (((m == -INFINITY) ? 0.f : m) + __log2f(l)) * kLn2 : -INFINITY;
+            constexpr bool partial = kSplit;
+            const int64_t prow = ((static_cast<int64_t>(bx) * a.Hkv + head) * a.n_split + split) * (2 * BM) + t * BM + r;
             uint16_t *dst = a.out + (static_cast<int64_t>(tok) * a.Hq + hq) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -491,7 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = 0u;
                 }
-                if (row_ok) {
+                if (row_ok && partial) {
+                    float4 *p4 = reinterpret_cast<float4 *>(a.part_o + prow * D + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        p4[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                            __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+                } else if (row_ok) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
@@ -501,9 +524,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
             }
-            if (row_ok && a.lse) {
-                const float v = (owned && l > 0.f) ? (((m == -INFINITY) ? 0.f : m) + __log2f(l)) * kLn2 : -INFINITY;
-                a.lse[static_cast<int64_t>(hq) * a.rows + tok] = v;
+            if (row_ok && partial) {
+                a.part_lse[prow] = row_lse;
+            } else if (row_ok && a.lse) {
+                a.lse[static_cast<int64_t>(hq) * a.rows + tok] = row_lse;
             }
         }
     }
@@ -514,11 +538,107 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Merge of the prefix chunks (one request): block (u, q) with u = row pair * Hkv + kv head takes
+// output columns [32 q, 32 q + 32); thread = row of the pair's two M tiles.  O = sum_c w_c O_c /
+// sum_c w_c with w_c = exp(lse_c - max_c lse_c); the LSE (written by the q = 0 blocks) is
+// max + log(sum w).  Runs after the attention launch (stream order), so every partial is
+// complete.
+template <int D>
+__global__ void __launch_bounds__(2 * BM)
+    split_merge_kernel(const AttnArgs a, int nb)
+{
+    const int unit = blockIdx.x;
+    const int q = blockIdx.y;
+    const int bx = unit / a.Hkv, head = unit % a.Hkv;
+    const int t = threadIdx.x / BM, r = threadIdx.x % BM;
+    const int t0 = (nb - 1 - bx) * 2 * a.tpt;
+    const int tok = t0 + t * a.tpt + r / a.g;
+    const int hq = head * a.g + r % a.g;
+    if (r >= a.g * a.tpt || tok >= a.rows) return;
+    const int64_t row0 = static_cast<int64_t>(unit) * a.n_split * (2 * BM) + threadIdx.x;
+    float mx = -INFINITY;
+    for (int c = 0; c < a.n_split; ++c) mx = fmaxf(mx, __ldg(a.part_lse + row0 + c * (2 * BM)));
+    float wsum = 0.f;
+    if (mx != -INFINITY)
+        for (int c = 0; c < a.n_split; ++c) wsum += ptx::ex2((__ldg(a.part_lse + row0 + c * (2 * BM)) - mx) * kLog2e);
+    const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+    uint16_t *dst = a.out + (static_cast<int64_t>(tok) * a.Hq + hq) * D;
+    {
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+        for (int c = 0; c < a.n_split && mx != -INFINITY; ++c) {
+            const float lc = __ldg(a.part_lse + row0 + c * (2 * BM));
+            if (lc == -INFINITY) continue;
+            const float w = ptx::ex2((lc - mx) * kLog2e);
+            const float4 *p4 = reinterpret_cast<const float4 *>(a.part_o + (row0 + c * (2 * BM)) * D + q * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 v = __ldg(p4 + j);
+                acc[4 * j] = fmaf(w, v.x, acc[4 * j]);
+                acc[4 * j + 1] = fmaf(w, v.y, acc[4 * j + 1]);
+                acc[4 * j + 2] = fmaf(w, v.z, acc[4 * j + 2]);
+                acc[4 * j + 3] = fmaf(w, v.w, acc[4 * j + 3]);
+            }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = ptx::pack_bf16x2(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst + q * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    }
+    if (a.lse && q == 0) a.lse[static_cast<int64_t>(hq) * a.rows + tok] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+}
+
 }  // namespace
 }  // namespace blink
 
 namespace blink {
 namespace {
+
+constexpr int kMinSplitTiles = 4;  // prefix tiles a chunk keeps at least
+
+// Prefix chunks for a small grid: a single request with a prefix whose (row pair, kv head) units
+// fill at most half of the SMs gets its prefix cut into S >= 2 chunks of c >= kMinSplitTiles
+// tiles each, S * units at most one wave.  S = 1 otherwise.
+void choose_split(int64_t units, int n_pre, int sms, int &S, int &c)
+{
+    S = 1;
+    c = 1 << 30;
+    if (units < 1 || units * 2 > sms || n_pre < 2 * kMinSplitTiles) return;
+    const int64_t by_sms = sms / units, by_tiles = n_pre / kMinSplitTiles;
+    const int s = static_cast<int>(by_sms < by_tiles ? by_sms : by_tiles);
+    if (s < 2) return;
+    const int cc = (n_pre + s - 1) / s;
+    const int ss = (n_pre + cc - 1) / cc;
+    if (ss < 2) return;
+    S = ss;
+    c = cc;
+}
+
+// Workspace after the 256-byte header when the prefix is split: partial LSE [units][S][2 BM]
+// and partial O [units][S][2 BM][d] (fp32), each region 256-byte aligned.
+struct SplitLayout {
+    size_t lse, o, total;
+};
+
+SplitLayout split_layout(int64_t units, int S, int d)
+{
+    SplitLayout l{};
+    l.lse = kHeaderBytes;
+    l.o = l.lse + align_up(static_cast<size_t>(units) * S * 2 * BM * sizeof(float), 256);
+    l.total = l.o + align_up(static_cast<size_t>(units) * S * 2 * BM * d * sizeof(float), 256);
+    return l;
+}
+
+int sm_count_attention()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
 
 // Validates the common arguments, encodes the tensor maps and launches the kernel for the request
 // table already filled in `a` (n_req, req_row, req_pre, req_P).  The arena holds arena_slots
@@ -605,21 +725,49 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
     a.scale_log2 = sc * kLog2e;
 
-    dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(Hkv));
+    // A small grid over one request's prefix: split the prefix (if the workspace has the room).
+    a.n_split = 1;
+    a.split_tiles = 1 << 30;
+    a.part_o = nullptr;
+    a.part_lse = nullptr;
+    if (a.n_req == 1 && a.req_P[0] > 0) {
+        int S = 1, c = 1 << 30;
+        choose_split(blocks * Hkv, (a.req_P[0] + BN - 1) / BN, sm_count_attention(), S, c);
+        if (S > 1) {
+            const SplitLayout lay = split_layout(blocks * Hkv, S, d);
+            if (ws_bytes >= lay.total) {
+                auto *wsb = static_cast<uint8_t *>(d_ws);
+                a.n_split = S;
+                a.split_tiles = c;
+                a.part_lse = reinterpret_cast<float *>(wsb + lay.lse);
+                a.part_o = reinterpret_cast<float *>(wsb + lay.o);
+            }
+        }
+    }
+    if (blocks * a.n_split > 0x7FFFFFFF) return BLINK_OUT_OF_RANGE;
+    dim3 grid(static_cast<unsigned>(blocks * a.n_split), static_cast<unsigned>(Hkv));
     if (d == 128) {
         const int smem = Layout<128>::kAlloc;
-        if (cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
+        auto kern = a.n_split > 1 ? attention_kernel<128, true> : attention_kernel<128, false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return BLINK_CUDA_ERROR;
-        attention_kernel<128><<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
+        kern<<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
     } else {
         // Reserve enough shared memory that only one block fits per SM: each block takes all
         // 512 tensor-memory columns.
         const int smem = Layout<64>::kAlloc > 120 * 1024 ? Layout<64>::kAlloc : 120 * 1024;
-        if (cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
+        auto kern = a.n_split > 1 ? attention_kernel<64, true> : attention_kernel<64, false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return BLINK_CUDA_ERROR;
-        attention_kernel<64><<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
+        kern<<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
+    }
+    if (a.n_split > 1) {
+        if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+        const unsigned units = static_cast<unsigned>(blocks * Hkv);
+        if (d == 128)
+            split_merge_kernel<128><<<dim3(units, 128 / 32), 2 * BM, 0, stream>>>(a, static_cast<int>(blocks));
+        else
+            split_merge_kernel<64><<<dim3(units, 64 / 32), 2 * BM, 0, stream>>>(a, static_cast<int>(blocks));
     }
     if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
     return BLINK_OK;
@@ -630,13 +778,15 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
 
 extern "C" size_t blink_attention_workspace(int32_t rows, int32_t B, int32_t P, int32_t Hq, int32_t Hkv, int32_t d)
 {
-    (void)rows;
+    using namespace blink;
     (void)B;
-    (void)P;
-    (void)Hq;
-    (void)Hkv;
-    (void)d;
-    return blink::kHeaderBytes;
+    if (rows < 1 || P < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 64 && d != 128) || Hq / Hkv > BM)
+        return kHeaderBytes;
+    const int tpt = BM / (Hq / Hkv);
+    const int64_t blocks = ((static_cast<int64_t>(rows) + tpt - 1) / tpt + 1) / 2;
+    int S = 1, c = 1 << 30;
+    choose_split(blocks * Hkv, (P + BN - 1) / BN, sm_count_attention(), S, c);
+    return S > 1 ? split_layout(blocks * Hkv, S, d).total : kHeaderBytes;
 }
 
 extern "C" blink_status blink_prefix_tail_attention(const blink_bf16 *q, const blink_bf16 *k_pre,

@@ -163,3 +163,29 @@ def test_attention_several_requests_one_launch(Hq, Hkv, d):
                                  (cu[qi:qi + len(tails) + 1] - r0).astype(np.int32), r1 - r0, P, Hq, Hkv, d)
         compare_attention(sub, out[r0:r1], lse[:, r0:r1])
         qi += len(tails)
+
+
+@pytest.mark.parametrize("case", [
+    # name, P, lengths, Hq, Hkv, d, padded width (0: varlen)
+    ("one-question", 4096, [40], 8, 2, 128, 0),
+    ("three-padded-g5-d64", 3000, [5, 33, 17], 10, 2, 64, 48),
+    ("one-question-18k-shape", 18432, [64], 32, 8, 128, 0),
+], ids=lambda c: c[0])
+def test_attention_split_prefix_small_grid(case):
+    """A grid that fills a small part of the GPU (a single question against a long prefix) cuts
+    the prefix into chunks run by separate blocks; their partial outputs are merged by LSE, the
+    same merge as the prefix and tail parts.  Every row matches the oracle."""
+    name, P, lengths, Hq, Hkv, d, width = case
+    ins = wl.attention_inputs(_w(name, 500 + len(name), P, Hq, Hkv, d), lengths=np.array(lengths), P=P,
+                              padded_width=width or None)
+    rows = ins.rows
+    assert blink.attention_workspace_bytes(rows, len(lengths), P, Hq, Hkv, d) > 256  # the split path
+    out, lse, st = run_attention(ins, padded=bool(width))
+    assert st == blink.BLINK_OK
+    compare_attention(ins, out, lse)
+    if width:
+        owned = np.zeros(ins.rows, dtype=bool)
+        for s, L in zip(ins.seq_start, ins.seq_len):
+            owned[s:s + L] = True
+        assert (out[~owned] == 0).all()
+        assert np.isneginf(lse[:, ~owned]).all()
