@@ -22,6 +22,13 @@
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 // MMA issue order: S0(i), PV1(i-1), S1(i), PV0(i), so each softmax warpgroup works while the
 // tensor core runs the other tile's products.
+//
+// Small grids (one request whose blocks fill at most half of the SMs, e.g. one question against
+// a long prefix): the prefix tiles are cut into chunks, one block per (row pair, kv head, chunk);
+// each writes its partial O (normalised by its own sum) and LSE in fp32, the last chunk also runs
+// the tail tiles, and split_merge_kernel combines the chunks by LSE -- the same merge that joins
+// the prefix and tail parts.  The chunked form is a separate instantiation (kSplit), so the
+// common unsplit kernel carries none of it.
 #include <cstdint>
 
 #include "common.cuh"
