@@ -163,10 +163,10 @@ blink_status blink_kv_to_arena(const blink_bf16 *k_src, const blink_bf16 *v_src,
  * lse   [Hq, rows]       optional (may be NULL): fp32 natural-log log-sum-exp of each row
  * d_ws, ws_bytes         workspace of at least blink_attention_workspace(...) bytes, zero-filled
  *                        before its first use; the first word is the device error word
- * Small grids: when the (token-pair, kv head) blocks fill at most half of the GPU's SMs, the
- * prefix is cut into chunks of at least 4 key tiles run by separate blocks, and their partial
- * outputs are merged by LSE in a second launch (the merge of the prefix and tail parts, applied
- * again).  blink_attention_workspace then includes room for the fp32 partials (it sizes them for
+ * Small grids (one request whose (token-pair, kv head) blocks leave SMs idle, e.g. a few
+ * questions against a long prefix): when a launch-time model predicts a clear gain, the prefix is
+ * cut into chunks of at least 4 key tiles run by separate blocks, and their partial outputs are
+ * merged by LSE in a second launch (the merge of the prefix and tail parts, applied again).  blink_attention_workspace then includes room for the fp32 partials (it sizes them for
  * the current device); with a smaller workspace the call runs unsplit.  Results agree with the
  * unsplit path within the rounding of the merge.
  * Errors: BLINK_INVALID_ARG, BLINK_OUT_OF_RANGE, BLINK_WORKSPACE_TOO_SMALL, BLINK_CUDA_ERROR;

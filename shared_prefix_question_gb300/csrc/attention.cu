@@ -606,22 +606,37 @@ namespace {
 
 constexpr int kMinSplitTiles = 4;  // prefix tiles a chunk keeps at least
 
-// Prefix chunks for a small grid: a single request with a prefix whose (row pair, kv head) units
-// fill at most half of the SMs gets its prefix cut into S >= 2 chunks of c >= kMinSplitTiles
-// tiles each, S * units at most one wave.  S = 1 otherwise.
-void choose_split(int64_t units, int n_pre, int sms, int &S, int &c)
+// Prefix chunks for a grid that leaves SMs idle (one request with a prefix).  Launch time is
+// modelled in KV-tile iterations: waves(units * S) * (chunk tiles + kFixedTiles), plus for S > 1
+// the merge launch and the fp32 partials written and read back (bytes / kBytesPerTile), where a
+// wave is one block per SM.  S >= 2 chunks of c >= kMinSplitTiles tiles are used when that beats
+// the unsplit launch by at least 10 % and the split grid stays within four waves.  S = 1
+// otherwise.  (Measured: one question against an 18k prefix runs 4x faster in 18 chunks; the 2k
+// workload, two waves of 160 blocks, runs 23 % slower in 2 chunks, which the model rejects.)
+void choose_split(int64_t units, int n_pre, int d, int sms, int &S, int &c)
 {
+    constexpr int64_t kFixedTiles = 4;             // block start, pipeline fill and epilogue
+    constexpr int64_t kMergeTiles = 2;             // the merge launch
+    constexpr int64_t kBytesPerTile = 9ll << 20;   // DRAM bytes moved in one iteration's time
     S = 1;
     c = 1 << 30;
-    if (units < 1 || units * 2 > sms || n_pre < 2 * kMinSplitTiles) return;
-    const int64_t by_sms = sms / units, by_tiles = n_pre / kMinSplitTiles;
-    const int s = static_cast<int>(by_sms < by_tiles ? by_sms : by_tiles);
-    if (s < 2) return;
-    const int cc = (n_pre + s - 1) / s;
-    const int ss = (n_pre + cc - 1) / cc;
-    if (ss < 2) return;
-    S = ss;
-    c = cc;
+    if (units < 1 || sms < 1 || n_pre < 2 * kMinSplitTiles) return;
+    auto waves = [&](int64_t u) { return (u + sms - 1) / sms; };
+    const int64_t unsplit = waves(units) * (n_pre + kFixedTiles);
+    int64_t best = unsplit * 9 / 10;  // a split has to win by 10 %
+    for (int s = 2; s <= n_pre / kMinSplitTiles; ++s) {
+        const int cc = (n_pre + s - 1) / s;
+        const int ss = (n_pre + cc - 1) / cc;
+        if (ss < 2 || ss != s) continue;  // each chunk count considered once, at its own size
+        if (units * ss > 4LL * sms) break;
+        const int64_t partial_bytes = units * ss * (2 * BM) * d * 8;  // fp32 O written and read
+        const int64_t cost = waves(units * ss) * (cc + kFixedTiles) + kMergeTiles + partial_bytes / kBytesPerTile;
+        if (cost < best) {
+            best = cost;
+            S = ss;
+            c = cc;
+        }
+    }
 }
 
 // Workspace after the 256-byte header when the prefix is split: partial LSE [units][S][2 BM]
@@ -739,7 +754,7 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
     a.part_lse = nullptr;
     if (a.n_req == 1 && a.req_P[0] > 0) {
         int S = 1, c = 1 << 30;
-        choose_split(blocks * Hkv, (a.req_P[0] + BN - 1) / BN, sm_count_attention(), S, c);
+        choose_split(blocks * Hkv, (a.req_P[0] + BN - 1) / BN, d, sm_count_attention(), S, c);
         if (S > 1) {
             const SplitLayout lay = split_layout(blocks * Hkv, S, d);
             if (ws_bytes >= lay.total) {
@@ -792,7 +807,7 @@ extern "C" size_t blink_attention_workspace(int32_t rows, int32_t B, int32_t P, 
     const int tpt = BM / (Hq / Hkv);
     const int64_t blocks = ((static_cast<int64_t>(rows) + tpt - 1) / tpt + 1) / 2;
     int S = 1, c = 1 << 30;
-    choose_split(blocks * Hkv, (P + BN - 1) / BN, sm_count_attention(), S, c);
+    choose_split(blocks * Hkv, (P + BN - 1) / BN, d, sm_count_attention(), S, c);
     return S > 1 ? split_layout(blocks * Hkv, S, d).total : kHeaderBytes;
 }
 
