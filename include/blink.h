@@ -66,6 +66,15 @@ const char *blink_status_string(blink_status s);
  * Returns BLINK_OK, BLINK_DEVICE_FLAG or BLINK_DEVICE_TIMEOUT (or BLINK_CUDA_ERROR). */
 blink_status blink_read_device_status(void *d_ws, int32_t clear, cudaStream_t stream);
 
+/* Self-test of the failure path every kernel relies on (no counterpart on the pages): one
+ * thread waits, with the library's bounded wait, on a barrier that nothing arrives at; after
+ * limit_us microseconds (1..1000000) the wait gives up and latches BLINK_DEVICE_TIMEOUT in the
+ * workspace's error word, exactly as a kernel whose copy or peer never arrived would.  Returns
+ * that status (BLINK_DEVICE_TIMEOUT when the path works), after clearing the word.  Nothing
+ * faults or traps and the context stays usable.  d_ws: a workspace of at least 256 bytes.
+ * Synchronises `stream`. */
+blink_status blink_selftest_wait_timeout(uint32_t limit_us, void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------------------------
  * Pack plan -- blink.py `_batches` (token-budget packing, shortest first, a forward closes when
  * (longest x count) would pass the padded-token budget or at the row cap; a sequence longer

@@ -46,6 +46,7 @@ _sz = ctypes.c_size_t
 _SIGNATURES = {
     "blink_status_string": (ctypes.c_char_p, [_i32]),
     "blink_read_device_status": (_i32, [_vp, _i32, _vp]),
+    "blink_selftest_wait_timeout": (_i32, [ctypes.c_uint32, _vp, _sz, _vp]),
     "blink_pack_plan": (_i32, [_vp, _i32, _i32, _i32] + [_vp] * 10 + [_vp]),
     "blink_attention_workspace": (_sz, [_i32] * 6),
     "blink_prefix_tail_attention": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -212,6 +213,12 @@ def blink_prefix_tail_attention_multi(q, k_arena, v_arena, k_tail, v_tail, cu_se
 
 def blink_read_device_status(ws: torch.Tensor, clear: bool = True, stream=None) -> int:
     return int(lib().blink_read_device_status(_ptr(ws), 1 if clear else 0, _stream(stream)))
+
+
+def blink_selftest_wait_timeout(limit_us: int, ws: torch.Tensor, stream=None) -> int:
+    """Runs the bounded device wait against a barrier nothing arrives at; returns the status it
+    latched (BLINK_DEVICE_TIMEOUT when the failure path works)."""
+    return int(lib().blink_selftest_wait_timeout(int(limit_us), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 # ------------------------------------------------------------------------------------------------ readout

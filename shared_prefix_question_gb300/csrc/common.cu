@@ -2,6 +2,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace blink {
 
@@ -71,4 +72,36 @@ extern "C" blink_status blink_read_device_status(void *d_ws, int32_t clear, cuda
     if (word == 0) return BLINK_OK;
     if (word == BLINK_DEVICE_TIMEOUT) return BLINK_DEVICE_TIMEOUT;
     return BLINK_DEVICE_FLAG;
+}
+
+namespace blink {
+namespace {
+
+// One thread waits, with the same bounded wait every kernel uses, on a barrier that nothing
+// arrives at; the wait gives up after limit_ns and latches BLINK_DEVICE_TIMEOUT.
+__global__ void selftest_wait_kernel(int *err, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_wait(&bar, 0, &abort_flag, err, BLINK_DEVICE_TIMEOUT, limit_ns);
+}
+
+}  // namespace
+}  // namespace blink
+
+extern "C" blink_status blink_selftest_wait_timeout(uint32_t limit_us, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    using namespace blink;
+    if (!d_ws) return BLINK_INVALID_ARG;
+    if (ws_bytes < kHeaderBytes) return BLINK_WORKSPACE_TOO_SMALL;
+    if (limit_us < 1 || limit_us > 1000000) return BLINK_OUT_OF_RANGE;
+    auto *hdr = static_cast<WorkspaceHeader *>(d_ws);
+    if (cudaMemsetAsync(&hdr->error, 0, sizeof(int32_t), stream) != cudaSuccess) return BLINK_CUDA_ERROR;
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(&hdr->error, static_cast<uint64_t>(limit_us) * 1000u);
+    if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+    return blink_read_device_status(d_ws, 1, stream);
 }

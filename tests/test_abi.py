@@ -99,3 +99,10 @@ def test_plan_host_checks(lib):
     assert L.blink_pack_plan(FAKE, 10, 100, -1, *f, None) == blink.BLINK_INVALID_ARG    # negative row cap
     assert L.blink_pack_plan(FAKE, 0, 100, 0, *f, None) == blink.BLINK_OUT_OF_RANGE
     assert L.blink_pack_plan(FAKE, 32769, 100, 0, *f, None) == blink.BLINK_OUT_OF_RANGE
+
+
+def test_selftest_wait_host_checks(lib):
+    assert lib.blink_selftest_wait_timeout(1000, None, 256, None) == blink.BLINK_INVALID_ARG
+    assert lib.blink_selftest_wait_timeout(1000, FAKE, 16, None) == blink.BLINK_WORKSPACE_TOO_SMALL
+    assert lib.blink_selftest_wait_timeout(0, FAKE, 256, None) == blink.BLINK_OUT_OF_RANGE
+    assert lib.blink_selftest_wait_timeout(2000000, FAKE, 256, None) == blink.BLINK_OUT_OF_RANGE

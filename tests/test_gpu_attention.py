@@ -189,3 +189,19 @@ def test_attention_split_prefix_small_grid(case):
             owned[s:s + L] = True
         assert (out[~owned] == 0).all()
         assert np.isneginf(lse[:, ~owned]).all()
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """Every wait inside the kernels is bounded: one that never completes gives up, latches
+    BLINK_DEVICE_TIMEOUT in the workspace's error word and returns, with nothing faulted.  The
+    self-test waits on a barrier nothing arrives at (5 ms limit); afterwards the same workspace
+    and context run an attention call that matches the oracle."""
+    ws = blink.new_workspace(256, torch.device("cuda"))
+    t0 = __import__("time").perf_counter()
+    assert blink.blink_selftest_wait_timeout(5000, ws) == blink.BLINK_DEVICE_TIMEOUT
+    assert __import__("time").perf_counter() - t0 < 5.0
+    assert blink.blink_read_device_status(ws) == blink.BLINK_OK  # the self-test cleared the word
+    ins = wl.attention_inputs(_w("after-timeout", 600, 64, 4, 2, 64), lengths=np.array([8, 12]), P=64)
+    out, lse, st = run_attention(ins)
+    assert st == blink.BLINK_OK
+    compare_attention(ins, out, lse)
