@@ -117,19 +117,22 @@ def test_attention_workloads(name, n_sample):
     assert np.isfinite(out[rows]).all()
 
 
+@pytest.mark.parametrize("long_prefix", [False, True])
 @pytest.mark.parametrize("Hq,Hkv,d", [(8, 2, 128), (10, 2, 128), (4, 2, 64)])
-def test_attention_several_requests_one_launch(Hq, Hkv, d):
+def test_attention_several_requests_one_launch(Hq, Hkv, d, long_prefix):
     """blink.py `logits_many` packs the questions of several requests into one forward; each
     request keeps its own prefix (a region of one KV arena, simit engine.py).  Every request's
     rows must equal the single-request oracle over that request's prefix."""
     from tests.helpers import dev_i32, host_f64
-    rng = np.random.default_rng(Hq * 7 + d)
+    rng = np.random.default_rng(Hq * 7 + d + 1000 * long_prefix)
     reqs = [  # (prefix length, tail lengths)
         (300, [17, 5, 40]),
         (0, [33, 2]),        # a request on the plain causal path
         (129, [1, 64, 9, 12]),
         (1000, [90]),
     ]
+    if long_prefix:  # one request long enough that the launch uses the two-tile kernel
+        reqs.append((3300, [30, 7]))
     stride = Hkv * d + 64
     starts, slot = [], 7
     for P, _ in reqs:
@@ -202,6 +205,20 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     assert __import__("time").perf_counter() - t0 < 5.0
     assert blink.blink_read_device_status(ws) == blink.BLINK_OK  # the self-test cleared the word
     ins = wl.attention_inputs(_w("after-timeout", 600, 64, 4, 2, 64), lengths=np.array([8, 12]), P=64)
+    out, lse, st = run_attention(ins)
+    assert st == blink.BLINK_OK
+    compare_attention(ins, out, lse)
+
+
+def test_attention_two_tile_kernel_all_rows():
+    """A prefix of 24 key tiles with short tails runs the two-tile kernel (a block's estimated KV
+    iterations exceed the single-tile limit) with enough blocks that the prefix is not split;
+    every row matches the oracle.  (The small cases above, with a short prefix, run the
+    single-tile kernel.)"""
+    P, Hq, Hkv, d = 3072, 16, 8, 128
+    lengths = np.random.default_rng(41).integers(20, 49, size=40)
+    ins = wl.attention_inputs(_w("two-tile", 700, P, Hq, Hkv, d), lengths=lengths, P=P)
+    assert blink.attention_workspace_bytes(ins.rows, len(lengths), P, Hq, Hkv, d) == 256  # unsplit
     out, lse, st = run_attention(ins)
     assert st == blink.BLINK_OK
     compare_attention(ins, out, lse)
