@@ -6,6 +6,10 @@
 // The warp that completes a question's last row (an atomic ticket per question, no spinning)
 // then applies the temperature softmax over that question's logits in place.  Consecutive rows
 // of a block belong to the same question, so the hidden state is reused from L1.
+//
+// For large label counts (HBM-bound) the warps only write their logits and a second,
+// one-warp-per-question launch runs the softmaxes: waiting on the ticket's result lengthened
+// every warp more than the second launch costs.
 #include <cstdint>
 #include <mutex>
 
@@ -16,6 +20,8 @@ namespace blink {
 namespace {
 
 constexpr int kReadoutWarps = 8;
+// From this many labels on, the softmaxes run in a second launch instead of behind a ticket.
+constexpr int kSplitFinishLabels = 8192;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -76,6 +82,44 @@ __device__ __forceinline__ int question_of(const int32_t *__restrict__ off, int 
 
 // Six resident blocks per SM (at most 40 registers a thread): measured fastest on the HBM-bound
 // readout-stress input (65k random 10 KB rows) among 3 to 8 blocks.
+// Temperature softmax of question b's logits probs[lo, hi) in place, then the typed answer if
+// asked for (one warp).
+__device__ __forceinline__ void finish_question(int b, int lo, int hi, int lane, float log2e_over_t,
+                                                float *__restrict__ probs, const int32_t *__restrict__ qtype,
+                                                float *__restrict__ answers, int *__restrict__ err)
+{
+    float v[8];
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int k = lo + lane + 32 * j;
+        v[j] = k < hi ? __ldcg(probs + k) * log2e_over_t : -INFINITY;
+        m = fmaxf(m, v[j]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int k = lo + lane + 32 * j;
+        v[j] = k < hi ? exp2f(v[j] - m) : 0.f;
+        s += v[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    const float inv = 1.0f / s;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int k = lo + lane + 32 * j;
+        if (k < hi) probs[k] = v[j] * inv;
+    }
+    if (qtype && answers) write_answer(v, inv, hi - lo, lane, __ldg(qtype + b), answers + 3 * b, err);
+}
+
+// kFused: the warp that completes a question (atomic ticket) runs its softmax; otherwise every
+// warp only writes its logit and readout_finish_kernel runs the softmaxes afterwards (for large
+// label counts, where the ticket's wait on every warp costs more than a second launch).
+template <bool kFused>
 __global__ void __launch_bounds__(kReadoutWarps * 32, 6)
     readout_kernel(const uint16_t *__restrict__ hidden, int64_t hstride, int hidden_rows,
                    const int32_t *__restrict__ last_idx, const int32_t *__restrict__ slot_of,
@@ -139,6 +183,15 @@ __global__ void __launch_bounds__(kReadoutWarps * 32, 6)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
 
+    if (!kFused) {  // the logit is final here; readout_finish_kernel runs the softmax
+        if (lane == 0) {
+            const float z = bad ? __int_as_float(0x7FC00000) : acc;
+            probs[r] = z;
+            if (logits) logits[r] = z;
+            if (bad) atomicCAS(err, 0, BLINK_DEVICE_FLAG);
+        }
+        return;
+    }
     uint32_t ticket = 0;
     if (lane == 0) {
         const float z = bad ? __int_as_float(0x7FC00000) : acc;
@@ -150,34 +203,23 @@ __global__ void __launch_bounds__(kReadoutWarps * 32, 6)
     ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
     if (ticket != static_cast<uint32_t>(K - 1)) return;
 
-    // This warp completed question b: temperature softmax over its K staged logits.
+    // This warp completed question b: acquire every other row's staged logit, then finish.
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    float v[8];
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int k = lo + lane + 32 * j;
-        v[j] = k < hi ? __ldcg(probs + k) * log2e_over_t : -INFINITY;
-        m = fmaxf(m, v[j]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int k = lo + lane + 32 * j;
-        v[j] = k < hi ? exp2f(v[j] - m) : 0.f;
-        s += v[j];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    const float inv = 1.0f / s;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int k = lo + lane + 32 * j;
-        if (k < hi) probs[k] = v[j] * inv;
-    }
-    if (qtype && answers) write_answer(v, inv, K, lane, __ldg(qtype + b), answers + 3 * b, err);
+    finish_question(b, lo, hi, lane, log2e_over_t, probs, qtype, answers, err);
+}
+
+// One warp per question: the softmax (and answer) over the logits readout_kernel<false> wrote.
+__global__ void __launch_bounds__(kReadoutWarps * 32)
+    readout_finish_kernel(const int32_t *__restrict__ label_off, int B, int sum_k, float log2e_over_t,
+                          float *__restrict__ probs, const int32_t *__restrict__ qtype, float *__restrict__ answers,
+                          int *__restrict__ err)
+{
+    const int b = blockIdx.x * kReadoutWarps + (threadIdx.x >> 5);
+    if (b >= B) return;
+    const int lo = max(0, min(sum_k, __ldg(label_off + b)));
+    const int hi = max(lo, min(sum_k, __ldg(label_off + b + 1)));
+    if (hi - lo < 1 || hi - lo > BLINK_MAX_OPTIONS) return;  // flagged by the offsets check
+    finish_question(b, lo, hi, threadIdx.x & 31, log2e_over_t, probs, qtype, answers, err);
 }
 
 }  // namespace
@@ -212,14 +254,22 @@ extern "C" blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hi
 
     auto *hdr = static_cast<WorkspaceHeader *>(d_ws);
     auto *counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(d_ws) + kHeaderBytes);
-    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(B) * sizeof(uint32_t), stream) != cudaSuccess)
-        return BLINK_CUDA_ERROR;
     const int grid = (sum_k + kReadoutWarps - 1) / kReadoutWarps;
     const float log2e_over_t = kLog2e / temperature;
-    readout_kernel<<<grid, kReadoutWarps * 32, 0, stream>>>(hidden, hidden_row_stride, hidden_rows, d_last_idx,
-                                                           d_slot_of, unembed, V, H, d_label_off, d_label_ids, B, sum_k,
-                                                           log2e_over_t, d_probs, d_logits, d_qtype, d_answers,
-                                                           counters, &hdr->error);
+    if (sum_k >= kSplitFinishLabels) {  // no tickets: no counters to clear
+        readout_kernel<false><<<grid, kReadoutWarps * 32, 0, stream>>>(
+            hidden, hidden_row_stride, hidden_rows, d_last_idx, d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
+            sum_k, log2e_over_t, d_probs, d_logits, d_qtype, d_answers, counters, &hdr->error);
+        if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+        readout_finish_kernel<<<(B + kReadoutWarps - 1) / kReadoutWarps, kReadoutWarps * 32, 0, stream>>>(
+            d_label_off, B, sum_k, log2e_over_t, d_probs, d_qtype, d_answers, &hdr->error);
+    } else {
+        if (cudaMemsetAsync(counters, 0, static_cast<size_t>(B) * sizeof(uint32_t), stream) != cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        readout_kernel<true><<<grid, kReadoutWarps * 32, 0, stream>>>(
+            hidden, hidden_row_stride, hidden_rows, d_last_idx, d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
+            sum_k, log2e_over_t, d_probs, d_logits, d_qtype, d_answers, counters, &hdr->error);
+    }
     if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
     if (h_probs || h_answers) {
         int32_t word = 0;
@@ -296,7 +346,7 @@ extern "C" blink_status blink_label_readout_noalloc(const blink_bf16 *hidden, in
         cudaSuccess)
         return BLINK_CUDA_ERROR;
     const int grid = (sum_k + kReadoutWarps - 1) / kReadoutWarps;
-    readout_kernel<<<grid, kReadoutWarps * 32, 0, stream>>>(hidden, hidden_row_stride, hidden_rows, d_last_idx,
+    readout_kernel<true><<<grid, kReadoutWarps * 32, 0, stream>>>(hidden, hidden_row_stride, hidden_rows, d_last_idx,
                                                            d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
                                                            sum_k, kLog2e / temperature, d_probs, d_logits, nullptr,
                                                            nullptr, counters, err);

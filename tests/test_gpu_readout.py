@@ -142,15 +142,15 @@ def test_readout_answers(name):
 
 
 @pytest.mark.parametrize("with_slots", [False, True])
-def test_readout_rows_ordered_by_id_match_request_order(with_slots):
-    """Above 64 MiB of offered rows the readout first orders the labels so that those of one
-    vocabulary id run back to back (the repeats of a row then come from L2).  Each label's FP32
-    dot is the same sum in either order, so logits and probabilities equal, bit for bit, those
-    of the entry point that keeps request order, and they match the oracle.  Questions share a
-    pool of ids (blink.py `render` offers the first K labels of one pool) and some repeat an id
-    inside one question; H = 5128 leaves a ragged last batch of chunks."""
+def test_readout_two_launch_path_matches_fused(with_slots):
+    """From 8192 labels on, the readout writes every logit first and runs the softmaxes (and
+    answers) in a second launch, one warp per question; below that, the warp that completes a
+    question runs its softmax.  Both compute each label's FP32 dot and each softmax the same way,
+    so the workspace entry (two launches here) equals the no-alloc entry (fused) bit for bit, and
+    both match the oracle.  Questions share a pool of ids, some repeat an id inside one question,
+    and H = 5128 leaves a ragged last batch of chunks."""
     rng = np.random.default_rng(31 + with_slots)
-    H, V, B = 5128, 4000, 400
+    H, V, B = 5128, 4000, 500
     pool = rng.choice(V, 40, replace=False)
     ks = rng.integers(1, 41, size=B)
     parts = []
@@ -163,7 +163,7 @@ def test_readout_rows_ordered_by_id_match_request_order(with_slots):
             parts.append(rng.permutation(pool)[:k])
     off = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
     ids = np.concatenate(parts).astype(np.int32)
-    assert len(ids) * H * 2 > 64 << 20  # the ordered path
+    assert len(ids) >= 8192  # the two-launch path
     rows = B + 5
     hidden = wl.normal_bf16(rng, (rows, H))
     W = wl.normal_bf16(rng, (V, H), std=0.02)
@@ -176,17 +176,16 @@ def test_readout_rows_ordered_by_id_match_request_order(with_slots):
     d_hidden, d_W, d_off, d_ids = dev_bf16(hidden), dev_bf16(W), dev_i32(off), dev_i32(ids)
     d_last = dev_i32(per_slot if with_slots else last)
     d_slot = dev_i32(slot_of) if with_slots else None
-    lg_ordered = torch.empty(len(ids), dtype=torch.float32, device="cuda")
-    lg_request = torch.empty_like(lg_ordered)
-    p_ordered, ws = blink.blink_label_readout(d_hidden, d_last, d_W, d_off, d_ids, 0.7, logits=lg_ordered,
-                                              slot_of=d_slot)
-    p_request = blink.blink_label_readout_noalloc(d_hidden, d_last, d_W, d_off, d_ids, 0.7, logits=lg_request,
-                                                  slot_of=d_slot)
+    lg_two = torch.empty(len(ids), dtype=torch.float32, device="cuda")
+    lg_fused = torch.empty_like(lg_two)
+    p_two, ws = blink.blink_label_readout(d_hidden, d_last, d_W, d_off, d_ids, 0.7, logits=lg_two, slot_of=d_slot)
+    p_fused = blink.blink_label_readout_noalloc(d_hidden, d_last, d_W, d_off, d_ids, 0.7, logits=lg_fused,
+                                                slot_of=d_slot)
     torch.cuda.synchronize()
     assert blink.blink_read_device_status(ws) == blink.BLINK_OK
-    assert torch.equal(lg_ordered, lg_request)
-    assert torch.equal(p_ordered, p_request)
-    compare_readout(p_ordered.cpu().numpy().astype(np.float64), ins)
+    assert torch.equal(lg_two, lg_fused)
+    assert torch.equal(p_two, p_fused)
+    compare_readout(p_two.cpu().numpy().astype(np.float64), ins)
 
 
 @pytest.mark.parametrize("with_slots", [False, True])
