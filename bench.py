@@ -597,7 +597,8 @@ def readout_stress(blink, dev, hbm_peak, peak_kind, flush, args):
                                       "readout_stress"),
             "kernel": "readout_kernel", "ms": ms, "algorithmic_bytes": nbytes,
             "input": f"512 questions, {len(ids)} labels ({distinct} distinct rows) drawn per question without "
-                     f"replacement from {w.V}, hidden {w.H}; includes the counter memset",
+                     f"replacement from {w.V}, hidden {w.H}; the whole call is timed (logit launch and "
+                     f"softmax launch)",
             "peak_kind": f"{peak_kind} copy bandwidth"}
 
 
