@@ -210,15 +210,32 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     compare_attention(ins, out, lse)
 
 
-def test_attention_two_tile_kernel_all_rows():
-    """A prefix of 24 key tiles with short tails runs the two-tile kernel (a block's estimated KV
-    iterations exceed the single-tile limit) with enough blocks that the prefix is not split;
-    every row matches the oracle.  (The small cases above, with a short prefix, run the
-    single-tile kernel.)"""
-    P, Hq, Hkv, d = 3072, 16, 8, 128
-    lengths = np.random.default_rng(41).integers(20, 49, size=40)
-    ins = wl.attention_inputs(_w("two-tile", 700, P, Hq, Hkv, d), lengths=lengths, P=P)
+@pytest.mark.parametrize("case", [
+    # name, P, n tails, Hq, Hkv, padded width (0: varlen)
+    ("g2", 3072, 40, 16, 8, 0),
+    ("g5-padded", 2500, 61, 10, 2, 64),
+], ids=lambda c: c[0])
+def test_attention_two_tile_kernel_all_rows(case):
+    """A prefix of 20-24 key tiles with short tails runs the two-tile kernel (a block's estimated
+    KV iterations exceed the single-tile limit) with enough blocks that the prefix is not split;
+    every row matches the oracle.  Both cases end a kv head's blocks on a row pair whose second
+    tile starts past the last row; g = 5 leaves 3 of every 128 tile rows unused; the padded case
+    checks that rows no question owns stay zero with LSE -inf.  (The small cases above, with a
+    short prefix, run the single-tile kernel.)"""
+    name, P, n, Hq, Hkv, width = case
+    d = 128
+    lengths = np.random.default_rng(41 + n).integers(20, 49, size=n)
+    ins = wl.attention_inputs(_w("two-tile-" + name, 700 + n, P, Hq, Hkv, d), lengths=lengths, P=P,
+                              padded_width=width or None)
+    tpt = 128 // (Hq // Hkv)
+    assert (ins.rows + tpt - 1) // tpt % 2 == 1  # an odd tile count: the last block has one tile
     assert blink.attention_workspace_bytes(ins.rows, len(lengths), P, Hq, Hkv, d) == 256  # unsplit
-    out, lse, st = run_attention(ins)
+    out, lse, st = run_attention(ins, padded=bool(width))
     assert st == blink.BLINK_OK
     compare_attention(ins, out, lse)
+    if width:
+        owned = np.zeros(ins.rows, dtype=bool)
+        for s, L in zip(ins.seq_start, ins.seq_len):
+            owned[s:s + L] = True
+        assert (out[~owned] == 0).all()
+        assert np.isneginf(lse[:, ~owned]).all()
