@@ -51,6 +51,11 @@ constexpr uint32_t kTmemCols = 512;
 
 constexpr int kMaxRequests = 64;  // blink.py `Batcher.MAX_REQUESTS`
 
+template <int N>
+struct IntTag {
+    static constexpr int value = N;
+};
+
 struct AttnArgs {
     const int32_t *cu;         // [B+1]
     const int32_t *seq_start;  // [B] or nullptr (varlen)
@@ -160,8 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *kv_s = base + L::kKVOff;
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + L::kBarOff);
     uint64_t *q_full = bars + 0;
-    uint64_t *full = bars + 1;     // [4]
-    uint64_t *empty = bars + 5;    // [4]
+    uint64_t *full = bars + 1;     // [2] by iteration parity: that iteration's K and V tiles
+    uint64_t *empty = bars + 5;    // [4] per ring slot
     uint64_t *s_full = bars + 9;   // [2]
     uint64_t *p_full = bars + 11;  // [2]
     uint64_t *o_full = bars + 13;  // [2]
@@ -189,10 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         if (lane == 0) {
             ptx::mbar_init(q_full, 1);
-            for (int i = 0; i < kSlots; ++i) {
-                ptx::mbar_init(full + i, 1);
-                ptx::mbar_init(empty + i, 1);
-            }
+            for (int i = 0; i < 2; ++i) ptx::mbar_init(full + i, 2);  // the K and the V copy
+            for (int i = 0; i < kSlots; ++i) ptx::mbar_init(empty + i, 1);
             for (int t = 0; t < 2; ++t) {
                 ptx::mbar_init(s_full + t, 1);
                 ptx::mbar_init(p_full + t, 128);
@@ -271,38 +274,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------------- TMA producer
+        // K and V of iteration it go to slots 2 (it & 1) and 2 (it & 1) + 1 and both complete on
+        // full[it & 1], so the MMA thread waits once per iteration for its operands; each slot is
+        // released on its own (K after S_1, V after the product P_1 V) so neither copy waits for
+        // the other's use.
         if (lane == 0) {
             int n = 0;
             for (int it = 0; it < n_iter; ++it) {
                 const bool pre = it < n_pre;
                 const int kb = pre ? pre_start + (pre_lo + it) * BN : kbeg + (it - n_pre) * BN;
+                uint64_t *stage_full = full + (it & 1);
                 bool ok = true;
                 for (int kv = 0; kv < 2; ++kv) {
                     const int slot = n % kSlots;
                     const uint32_t ph = (n / kSlots) & 1;
                     if (!ptx::mbar_wait(empty + slot, ph ^ 1u, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)) {
+                        // giving up after the K copy: complete the iteration's arrival count so that
+                        // the drain below still sees that copy land
+                        if (kv == 1) ptx::mbar_arrive(stage_full);
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(full + slot, L::kKVTileBytes);
+                    ptx::mbar_arrive_expect_tx(stage_full, L::kKVTileBytes);
                     const CUtensorMap *map = pre ? (kv ? &tm_vpre : &tm_kpre) : (kv ? &tm_vtail : &tm_ktail);
                     for (int p = 0; p < L::kPanels; ++p)
                         ptx::tma_load_3d(kv_s + slot * L::kKVTileBytes + p * kHalfBytes, map, p * 64, head, kb,
-                                         full + slot);
+                                         stage_full);
                     ++n;
                 }
                 if (!ok) break;
             }
-            // Drain: every copy issued must have landed before the block may exit.
+            // Drain: every copy issued must have landed before the block may exit.  Copies of
+            // iterations before the last two were waited for by the MMA thread before their slots
+            // were reused.
             volatile int no_abort = 0;
             ptx::mbar_wait(q_full, 0, &no_abort, a.err, BLINK_DEVICE_TIMEOUT);
-            for (int j = n > kSlots ? n - kSlots : 0; j < n; ++j) {
+            const int n_it = (n + 1) / 2;  // iterations with at least their K copy issued
+            for (int j = n_it > 2 ? n_it - 2 : 0; j < n_it; ++j) {
                 no_abort = 0;
-                ptx::mbar_wait(full + (j % kSlots), (j / kSlots) & 1, &no_abort, a.err, BLINK_DEVICE_TIMEOUT);
+                ptx::mbar_wait(full + (j & 1), (j >> 1) & 1, &no_abort, a.err, BLINK_DEVICE_TIMEOUT);
             }
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
+        // The tensor core takes a product about when the previous one finishes, so whatever this
+        // thread does between two issues is idle tensor time: every operand address is built
+        // before the loop, the loop is unrolled by two so that the ring slots (K in 0 or 2, V in
+        // 1 or 3, by the iteration's parity) are compile-time, and each group of 8 products is
+        // issued from one asm block.
         if (lane == 0) {
             constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, true);
@@ -310,9 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t o_col[2] = {256u, 256u + D};
             const uint32_t q_addr[2] = {ptx::smem_u32(q_s0), ptx::smem_u32(q_s1)};
             const uint32_t kv_addr = ptx::smem_u32(kv_s);
-            // Every shared-memory descriptor the loop needs, built once: Q tiles, the two K slots
-            // and the two V slots, per 16-wide k-step.
             uint64_t qd[2][D / 16], kd[2][D / 16], vd[2][BN / 16];
+            uint32_t pa[2][BN / 16];  // P_t columns of each k-step (bf16 pairs: 8 columns per 16 keys)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
@@ -325,46 +343,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < BN / 16; ++kk) {
                 vd[0][kk] = ptx::smem_desc_sw128(kv_addr + 1 * L::kKVTileBytes + kk * 2048, kHalfBytes, 1024);
                 vd[1][kk] = ptx::smem_desc_sw128(kv_addr + 3 * L::kKVTileBytes + kk * 2048, kHalfBytes, 1024);
+                pa[0][kk] = tmem + s_col[0] + kk * 8;
+                pa[1][kk] = tmem + s_col[1] + kk * 8;
             }
-            auto qk = [&](int t, uint32_t k_addr) {
-                const bool hi = k_addr != kv_addr;  // K lives in slot 0 or slot 2
+            auto qk = [&](int t, int par) {
+                if constexpr (D == 128) {
+                    ptx::mma_ss_x8(tmem + s_col[t], qd[t], kd[par], idesc_s, 0u);
+                } else {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::mma_ss(tmem + s_col[t], qd[t][kk], hi ? kd[1][kk] : kd[0][kk], idesc_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        ptx::mma_ss(tmem + s_col[t], qd[t][kk], kd[par][kk], idesc_s, kk > 0 ? 1u : 0u);
+                }
             };
-            auto pv = [&](int t, uint32_t v_addr, bool first) {
-                const bool hi = v_addr != kv_addr + L::kKVTileBytes;  // V lives in slot 1 or slot 3
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    ptx::mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8, hi ? vd[1][kk] : vd[0][kk], idesc_pv,
-                                (!first || kk > 0) ? 1u : 0u);
+            auto pv = [&](int t, int par, bool first) {
+                ptx::mma_ts_x8(tmem + o_col[t], pa[t], vd[par], idesc_pv, first ? 0u : 1u);
+            };
+            // One KV iteration; kPar = i & 1 selects the slots.
+            auto step = [&](auto par_tag, int i) -> bool {
+                constexpr int kPar = decltype(par_tag)::value;
+                constexpr int kslot = 2 * kPar, prev_vslot = 3 - 2 * kPar;
+                // K and V of this iteration (one barrier per iteration parity)
+                if (!ptx::mbar_wait(full + kPar, (i >> 1) & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)) return false;
+                ptx::tc_fence_after();
+                qk(0, kPar);
+                ptx::mma_commit(s_full + 0);
+                if (i > 0) {
+                    if (!ptx::mbar_wait(p_full + 1, (i - 1) & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT))
+                        return false;
+                    ptx::tc_fence_after();
+                    pv(1, 1 - kPar, i == 1);
+                    ptx::mma_commit(empty + prev_vslot);
+                }
+                qk(1, kPar);
+                ptx::mma_commit(s_full + 1);
+                ptx::mma_commit(empty + kslot);
+                if (!ptx::mbar_wait(p_full + 0, i & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)) return false;
+                ptx::tc_fence_after();
+                pv(0, kPar, i == 0);
+                if (i == n_iter - 1) ptx::mma_commit(o_full + 0);
+                return true;
             };
             bool ok = ptx::mbar_wait(q_full, 0, abort_flag, a.err, BLINK_DEVICE_TIMEOUT);
             ptx::tc_fence_after();
-            for (int i = 0; ok && i < n_iter; ++i) {
-                const int kslot = (2 * i) % kSlots, vslot = (2 * i + 1) % kSlots;
-                const uint32_t kph = ((2 * i) / kSlots) & 1, vph = ((2 * i + 1) / kSlots) & 1;
-                if (!(ok = ptx::mbar_wait(full + kslot, kph, abort_flag, a.err, BLINK_DEVICE_TIMEOUT))) break;
-                ptx::tc_fence_after();
-                const uint32_t k_addr = kv_addr + kslot * L::kKVTileBytes;
-                qk(0, k_addr);
-                ptx::mma_commit(s_full + 0);
-                if (i > 0) {
-                    const int pvslot = (2 * (i - 1) + 1) % kSlots;
-                    if (!(ok = ptx::mbar_wait(p_full + 1, (i - 1) & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)))
-                        break;
-                    ptx::tc_fence_after();
-                    pv(1, kv_addr + pvslot * L::kKVTileBytes, i - 1 == 0);
-                    ptx::mma_commit(empty + pvslot);
-                }
-                qk(1, k_addr);
-                ptx::mma_commit(s_full + 1);
-                ptx::mma_commit(empty + kslot);
-                if (!(ok = ptx::mbar_wait(p_full + 0, i & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT))) break;
-                if (!(ok = ptx::mbar_wait(full + vslot, vph, abort_flag, a.err, BLINK_DEVICE_TIMEOUT))) break;
-                ptx::tc_fence_after();
-                pv(0, kv_addr + vslot * L::kKVTileBytes, i == 0);
-                if (i == n_iter - 1) ptx::mma_commit(o_full + 0);
+            for (int i = 0; ok && i < n_iter; i += 2) {
+                ok = step(IntTag<0>{}, i);
+                if (ok && i + 1 < n_iter) ok = step(IntTag<1>{}, i + 1);
             }
             if (ok) {
                 if (n_iter > 0) {
@@ -372,7 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int vslot = (2 * i + 1) % kSlots;
                     if (ptx::mbar_wait(p_full + 1, i & 1, abort_flag, a.err, BLINK_DEVICE_TIMEOUT)) {
                         ptx::tc_fence_after();
-                        pv(1, kv_addr + vslot * L::kKVTileBytes, i == 0);
+                        if (i & 1)
+                            pv(1, 1, i == 0);
+                        else
+                            pv(1, 0, i == 0);
                         ptx::mma_commit(empty + vslot);
                         ptx::mma_commit(o_full + 1);
                     }

@@ -62,13 +62,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the same condition (returns sooner than try_wait when the phase is done).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after `limit_ns` (or as soon
 // as *abort is set by another thread of the block); on giving up it sets *abort, records
 // `timeout_code` in *err and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
                                           int timeout_code, uint64_t limit_ns = 1000000000ull)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -152,6 +166,51 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Eight products into one accumulator, issued back to back from one asm block (nothing between
+// them for the issuing thread to execute): D (+)= sum_k A_k * B_k^T over the 8 k-steps, the first
+// step accumulating onto D only if `accumulate`.  The tensor core accepts a product about when the
+// previous one finishes, so any instruction between two issues is a gap in the tensor pipe.
+__device__ __forceinline__ void mma_ss_x8(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.b32 p, %18, 0;\n\t"
+        "setp.eq.b32 t, %18, %18;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, t;\n\t}" ::"r"(d_tmem),
+        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]),
+        "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same with A read from tensor memory (a[k] = column address of k-step k).
+__device__ __forceinline__ void mma_ts_x8(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.b32 p, %18, 0;\n\t"
+        "setp.eq.b32 t, %18, %18;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, t;\n\t}" ::"r"(d_tmem),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]),
+        "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
