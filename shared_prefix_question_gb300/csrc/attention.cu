@@ -472,13 +472,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j < lo_j || j > hi_j) s[j] = -INFINITY;
                 }
             }
-            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+            // row max, three operands per instruction, four independent chains
+            float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-            for (int j = 4; j < BN; j += 4) {
-                mx0 = fmaxf(mx0, s[j]);
-                mx1 = fmaxf(mx1, s[j + 1]);
-                mx2 = fmaxf(mx2, s[j + 2]);
-                mx3 = fmaxf(mx3, s[j + 3]);
+            for (int j = 8; j < BN; j += 8) {
+                mx0 = ptx::max3(mx0, s[j], s[j + 1]);
+                mx1 = ptx::max3(mx1, s[j + 2], s[j + 3]);
+                mx2 = ptx::max3(mx2, s[j + 4], s[j + 5]);
+                mx3 = ptx::max3(mx3, s[j + 6], s[j + 7]);
             }
             const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
             const bool need = m_new > m + kRescaleThreshold;
@@ -490,21 +491,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = m_new;
             }
             const float m_use = (m == -INFINITY) ? 0.f : m;
-            float rs0 = 0.f, rs1 = 0.f;
+            if constexpr (D == 128) {
+                // The softmax warps are bound by instruction issue, not by the exp2 unit: the
+                // exponent arguments of an element pair take one f32x2 fma (bit-identical to two
+                // fmaf), and four row-sum chains keep the adds from waiting on each other.
+                const uint64_t sl2x2 = ptx::f32x2(sl2, sl2), negm_x2 = ptx::f32x2(-m_use, -m_use);
+                float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t pk[32];
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float p0 = ptx::ex2(fmaf(s[c * 64 + 2 * j], sl2, -m_use));
-                    const float p1 = ptx::ex2(fmaf(s[c * 64 + 2 * j + 1], sl2, -m_use));
-                    rs0 += p0;
-                    rs1 += p1;
-                    pk[j] = ptx::pack_bf16x2(p0, p1);
+                    for (int j = 0; j < 32; ++j) {
+                        const uint64_t s2 = ptx::f32x2(s[c * 64 + 2 * j], s[c * 64 + 2 * j + 1]);
+                        float x0, x1;
+                        ptx::f32x2_split(ptx::fma_f32x2(s2, sl2x2, negm_x2), x0, x1);
+                        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                        if (j & 1) {
+                            rs2 += p0;
+                            rs3 += p1;
+                        } else {
+                            rs0 += p0;
+                            rs1 += p1;
+                        }
+                        pk[j] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st32(trow + s_col + c * 32, pk);
                 }
-                ptx::tmem_st32(trow + s_col + c * 32, pk);
+                l += (rs0 + rs2) + (rs1 + rs3);
+            } else {  // d = 64: the scalar form (the packed one costs this instantiation spills)
+                float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float p0 = ptx::ex2(fmaf(s[c * 64 + 2 * j], sl2, -m_use));
+                        const float p1 = ptx::ex2(fmaf(s[c * 64 + 2 * j + 1], sl2, -m_use));
+                        rs0 += p0;
+                        rs1 += p1;
+                        pk[j] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st32(trow + s_col + c * 32, pk);
+                }
+                l += rs0 + rs1;
             }
-            l += rs0 + rs1;
             // O_t still holds the sum up to the previous tile (that product completed before this
             // tile's scores were signalled); scale it to the new max before P_t is released.
             if (rescale && i > 0) {
