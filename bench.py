@@ -50,9 +50,17 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle sample")
+    ap.add_argument("--no-cpu-configs", action="store_true",
+                    help="skip the oracle timings on every workload of the table (about a minute of CPU work)")
     ap.add_argument("--no-rows", action="store_true", help="skip the measurements of the other path rows")
-    ap.add_argument("--only", choices=["readout_stress"], default=None,
-                    help="run one sub-measurement alone (for profiling) and print its JSON")
+    ap.add_argument("--only", choices=["readout_stress", "attention", "pack_plan"], default=None,
+                    help="run one sub-measurement alone (for profiling) and print its JSON: the readout on "
+                         "its stress input, the attention on --workload (optionally --questions / --tails), or "
+                         "the pack plan at 32768 lengths")
+    ap.add_argument("--questions", type=int, default=0,
+                    help="with --only attention: the first N questions of the workload (0: all)")
+    ap.add_argument("--tails", default="",
+                    help="with --only attention: comma-separated tail lengths instead of the workload's")
     return ap.parse_args()
 
 
@@ -201,6 +209,69 @@ def cpu_baseline(w, lengths, ins, rd, target_s: float, n_threads: int = 0):
                                       f"core ({t_one:.1f} s), scaled to the mean tail length"}}, q, tq
 
 
+def _oracle_flops(ins, tok, head):
+    """Algorithmic FLOPs of the oracle's attention rows (token, head): 4 d (P + i + 1) each."""
+    owner = np.searchsorted(ins.seq_start, tok, side="right") - 1
+    i = tok - ins.seq_start[owner]
+    return float(4.0 * ins.d * (ins.P + i + 1).astype(np.float64).sum())
+
+
+def cpu_baseline_per_config(cores: int, max_questions: int = 2, names=("tiny", "2k", "18k", "plain", "max")):
+    """The oracle, as it stands, on every workload of the table: the plan, the attention of every
+    tail row and head, and the label readout of every question.  Tiny, 2k, 18k and plain run in
+    full on all host cores; the largest request on its first `max_questions` questions (plan and
+    readout over all), extrapolated to all 512 by attention FLOPs.  Beside each, one core on a
+    sample (the attention of question 0's last 8 tail rows, every head), scaled by FLOPs to the
+    whole workload."""
+    from oracle import oracle
+    from shared_prefix_question_gb300 import workloads as wl
+    out = {}
+    for name in names:
+        w = wl.WORKLOADS[name]
+        lengths = wl.tail_lengths(w)
+        ins = wl.attention_inputs(w, lengths=lengths)
+        rd = wl.readout_inputs(w, rows=ins.rows)
+        total_flops = attention_flops(lengths, w.P, w.Hq, w.d)
+        q = w.n if name != "max" else max_questions
+        t0 = time.perf_counter()
+        oracle.pack_plan(lengths, wl.TOKEN_BUDGET, 0)
+        if q == w.n:
+            oracle.prefix_tail_attention(ins.q, ins.k_pre, ins.v_pre, ins.k_tail, ins.v_tail, ins.seq_start,
+                                         ins.seq_len, ins.P, ins.Hq, ins.Hkv, ins.d, n_threads=cores)
+            sub_flops = total_flops
+        else:
+            toks = np.concatenate([np.arange(ins.seq_start[b], ins.seq_start[b] + ins.seq_len[b]) for b in range(q)])
+            tok = np.repeat(toks, ins.Hq).astype(np.int32)
+            head = np.tile(np.arange(ins.Hq), len(toks)).astype(np.int32)
+            oracle.prefix_tail_attention(ins.q, ins.k_pre, ins.v_pre, ins.k_tail, ins.v_tail, ins.seq_start,
+                                         ins.seq_len, ins.P, ins.Hq, ins.Hkv, ins.d, select=(tok, head),
+                                         n_threads=cores)
+            sub_flops = _oracle_flops(ins, tok, head)
+        oracle.label_readout(rd.hidden, rd.last_idx, rd.unembed, rd.label_off, rd.label_ids, rd.temperature)
+        t = time.perf_counter() - t0
+        t_full = t * total_flops / sub_flops  # the plan and readout are < 1 % of the oracle's time
+        # one core: question 0's last 8 tail rows, every head
+        L0 = int(ins.seq_len[0])
+        toks = np.arange(ins.seq_start[0] + max(0, L0 - 8), ins.seq_start[0] + L0)
+        tok = np.repeat(toks, ins.Hq).astype(np.int32)
+        head = np.tile(np.arange(ins.Hq), len(toks)).astype(np.int32)
+        t1 = time.perf_counter()
+        oracle.prefix_tail_attention(ins.q, ins.k_pre, ins.v_pre, ins.k_tail, ins.v_tail, ins.seq_start,
+                                     ins.seq_len, ins.P, ins.Hq, ins.Hkv, ins.d, select=(tok, head), n_threads=1)
+        t1 = time.perf_counter() - t1
+        rate1 = _oracle_flops(ins, tok, head) / max(t1, 1e-9)
+        prefill = w.P + int(lengths.sum())
+        out[name] = {"questions_per_s": w.n / t_full, "prefill_tokens_per_s": prefill / t_full,
+                     "seconds": t, "cores": cores,
+                     "timed": "in full" if q == w.n else
+                              f"first {q} of {w.n} questions ({sub_flops:.3g} of {total_flops:.3g} attention FLOP), "
+                              f"extrapolated by FLOPs to {t_full:.0f} s",
+                     "single_core_questions_per_s": w.n / (total_flops / rate1),
+                     "single_core_sample": f"{len(toks)} tail rows x {ins.Hq} heads of question 0 in {t1:.2f} s "
+                                           f"({rate1 / 1e9:.2f} GFLOP/s), scaled by FLOPs"}
+    return out
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -260,6 +331,22 @@ def main():
     if args.only == "readout_stress":
         flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
         print(json.dumps(readout_stress(blink, dev, hbm_peak, peak_kind, flush, args)), flush=True)
+        return
+    if args.only == "attention":
+        from shared_prefix_question_gb300 import workloads as wl
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        if args.tails:
+            lengths = np.array([int(x) for x in args.tails.split(",")], dtype=np.int32)
+        else:
+            lengths = wl.tail_lengths(wl.WORKLOADS[args.workload]).astype(np.int32)
+            if args.questions:
+                lengths = lengths[:args.questions]
+        row = attention_config_row(blink, dev, args.workload, tc_peak, hbm_peak, flush, lengths=lengths)
+        print(json.dumps({"only": "attention", "workload": args.workload, **row}), flush=True)
+        return
+    if args.only == "pack_plan":
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        print(json.dumps({"only": "pack_plan", **pack_plan_row(blink, dev, flush)}), flush=True)
         return
 
     w, lengths, ins, rd = build_workload(args.workload)
@@ -385,6 +472,8 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, lengths, ins, rd, args.cpu_seconds)[0]
+            if not args.no_cpu_configs:
+                line["cpu_baseline"]["per_config"] = cpu_baseline_per_config(os.cpu_count())
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -529,11 +618,7 @@ def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
     out["several_requests"] = {"ms": ms, "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / tc_peak,
                                "shape": f"{n_req} requests x (prefix {Pr}, 16 tails U[32,128]) in one launch"}
     # 5. the pack plan at its largest size: 64 requests x 512 questions (32768 lengths U[16,1024])
-    plan_len = torch.randint(16, 1025, (32768,), generator=g, device=dev, dtype=torch.int32)
-    pout = None
-    pout = blink.blink_pack_plan(plan_len, 32768, 0, out=pout)
-    ms = _time(lambda: blink.blink_pack_plan(plan_len, 32768, 0, out=pout, sync=False), flush)
-    out["pack_plan_32768"] = {"ms": ms, "shape": "32768 lengths U[16,1024], budget 32768 (64 requests x 512)"}
+    out["pack_plan_32768"] = pack_plan_row(blink, dev, flush)
     # 6. log-space readout over option orders: 512 questions x 4 orders x up to 26 options
     B = 512
     K = rng.integers(2, 27, size=B)
@@ -554,6 +639,17 @@ def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
                                                    probs=pr, ws=dws, sum_k=sk), flush)
     out["rotation_debias"] = {"ms": ms, "shape": f"{B} questions x {R} orders x 2-26 options"}
     return out
+
+
+def pack_plan_row(blink, dev, flush):
+    """The pack plan at its largest size: 64 requests x 512 questions (32768 lengths U[16,1024])."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(12)
+    plan_len = torch.randint(16, 1025, (32768,), generator=g, device=dev, dtype=torch.int32)
+    pout = blink.blink_pack_plan(plan_len, 32768, 0)
+    ms = _time(lambda: blink.blink_pack_plan(plan_len, 32768, 0, out=pout, sync=False), flush)
+    return {"ms": ms, "shape": "32768 lengths U[16,1024], budget 32768 (64 requests x 512)"}
 
 
 def wl_tail_lengths(w):

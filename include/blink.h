@@ -99,8 +99,14 @@ blink_status blink_selftest_wait_timeout(uint32_t limit_us, void *d_ws, size_t w
  *                          when given, the call synchronises the stream.
  * Errors: BLINK_INVALID_ARG (null output, budget < 1, max_rows < 0), BLINK_OUT_OF_RANGE (n),
  * BLINK_DEVICE_FLAG (only with h_n_forwards: a length out of range), BLINK_CUDA_ERROR.
- * The planner is one thread block; it uses no workspace.
+ * Up to 2048 lengths the whole plan is one thread block.  Above that, the stable sort runs over
+ * the whole GPU first (blocks sort runs of 1024 keys, then merge rounds), with d_fwd_of_slot and
+ * d_last_padded as its two ping-pong buffers; the one-block plan kernel reads the sorted keys
+ * before it writes those outputs.  So the planner needs no workspace of its own:
+ * blink_pack_plan_workspace() returns 0 for every n.
  * ------------------------------------------------------------------------------------------ */
+size_t blink_pack_plan_workspace(int32_t n);
+
 blink_status blink_pack_plan(const int32_t *d_lengths, int32_t n, int32_t budget, int32_t max_rows,
                              int32_t *d_order, int32_t *d_slot_of, int32_t *d_fwd_of_slot, int32_t *d_fwd_slot_start,
                              int32_t *d_fwd_width, int32_t *d_cu_seqlens, int32_t *d_last_varlen,
@@ -309,7 +315,12 @@ blink_status blink_rotation_debias(const float *d_logits, const int32_t *d_pass_
  * library keeps until the process exits.
  *   - B above BLINK_STATIC_SCRATCH_QUESTIONS returns BLINK_OUT_OF_RANGE; nothing is launched.
  *   - The first call on a device looks up the array's device address with that device current
- *     (cudaGetSymbolAddress); make that first call before any stream capture on the device.
+ *     (cudaGetSymbolAddress); make that first call before any stream capture on the device.  The
+ *     address is kept per device and context: after a device reset (a new context, so a new copy
+ *     of the array) the next call looks it up again, and that call too should come before any
+ *     capture.
+ *   - From 8192 labels on, the softmaxes run in a second launch (as in blink_label_readout), so
+ *     only the error word is used; below that, one ticket per question as well.
  *   - Every call first clears the array's error word and tickets on `stream`.  All calls share
  *     the one array, which keeps the last call's contents: calls whose work can overlap on the
  *     GPU (different streams with no ordering between them) race, and must not be made.

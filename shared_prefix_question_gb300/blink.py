@@ -47,6 +47,7 @@ _SIGNATURES = {
     "blink_status_string": (ctypes.c_char_p, [_i32]),
     "blink_read_device_status": (_i32, [_vp, _i32, _vp]),
     "blink_selftest_wait_timeout": (_i32, [ctypes.c_uint32, _vp, _sz, _vp]),
+    "blink_pack_plan_workspace": (_sz, [_i32]),
     "blink_pack_plan": (_i32, [_vp, _i32, _i32, _i32] + [_vp] * 10 + [_vp]),
     "blink_attention_workspace": (_sz, [_i32] * 6),
     "blink_prefix_tail_attention": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -141,6 +142,11 @@ def blink_pack_plan(lengths: torch.Tensor, budget: int, max_rows: int = 0, out: 
 
 
 # ------------------------------------------------------------------------------------------------ attention
+def pack_plan_workspace_bytes(n: int) -> int:
+    """0: the planner's scratch is its own output arrays."""
+    return int(lib().blink_pack_plan_workspace(n))
+
+
 def attention_workspace_bytes(rows, B, P, Hq, Hkv, d) -> int:
     return int(lib().blink_attention_workspace(rows, B, P, Hq, Hkv, d))
 
@@ -260,7 +266,12 @@ def blink_label_readout_noalloc(hidden, last_idx, unembed, label_off, label_ids,
                                 host_probs=None, logits=None, slot_of=None, stream=None):
     """The readout for callers that cannot allocate device memory (the library keeps its scratch in a
     static device array; at most 32768 questions; calls that overlap on the GPU race).  Outputs are
-    allocated here only when the caller passes none."""
+    allocated here only when the caller passes none.
+
+    Device-side errors (a label id outside [0, V), malformed offsets) are reported only when
+    `host_probs` is given: the C call then reads the error word back after its copy and this
+    wrapper raises BlinkError.  Without `host_probs` the call stays asynchronous and such a
+    question's probabilities come back as NaN (or, for malformed offsets, unwritten)."""
     _need_cuda(hidden, last_idx, unembed, label_off, label_ids, probs, logits, slot_of)
     rows, H = hidden.shape
     V = unembed.shape[0]

@@ -322,6 +322,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
 }  // namespace
 }  // namespace blink
 
+// The plan's scratch is its own output arrays (the whole-GPU sort ping-pongs between
+// d_fwd_of_slot and d_last_padded before the plan kernel writes them), so no workspace.
+extern "C" size_t blink_pack_plan_workspace(int32_t n)
+{
+    (void)n;
+    return 0;
+}
+
 extern "C" blink_status blink_pack_plan(const int32_t *d_lengths, int32_t n, int32_t budget, int32_t max_rows,
                                         int32_t *d_order, int32_t *d_slot_of, int32_t *d_fwd_of_slot,
                                         int32_t *d_fwd_slot_start,

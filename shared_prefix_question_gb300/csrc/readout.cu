@@ -299,20 +299,53 @@ constexpr int kStaticHeaderWords = 64;  // 256 bytes: the error word, then reser
 // Held by every GPU that loads the library, until the process exits.
 static __device__ __align__(256) uint32_t g_readout_scratch[kStaticHeaderWords + BLINK_STATIC_SCRATCH_QUESTIONS];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Identifier of the current context (0 if the driver cannot say).  A device reset or a new
+// context on the same ordinal loads the module again, at a new address, under a new identifier.
+unsigned long long current_context_id()
+{
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 std::mutex g_scratch_mutex;
 void *g_scratch_addr[kStaticMaxDevices] = {};
+unsigned long long g_scratch_ctx[kStaticMaxDevices] = {};
 
-// Device address of g_readout_scratch on the current device, looked up once per device (the
-// array's name is only a host-side stand-in in host code).
+// Device address of g_readout_scratch in the current device's context (the array's name is
+// only a host-side stand-in in host code).  Looked up once per device and context: the first
+// call on a device, and the first after a device reset, look it up again.
 void *scratch_address()
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices) return nullptr;
+    // 0 before the runtime has made the device's context current (the lookup below does that)
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_readout_scratch) != cudaSuccess) return nullptr;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = current_context_id();
     }
     return g_scratch_addr[dev];
 }
@@ -341,15 +374,25 @@ extern "C" blink_status blink_label_readout_noalloc(const blink_bf16 *hidden, in
     if (!scratch) return BLINK_CUDA_ERROR;
     auto *err = static_cast<int *>(scratch);
     auto *counters = static_cast<uint32_t *>(scratch) + kStaticHeaderWords;
-    // Calls share the array: clear this call's error word and tickets first.
-    if (cudaMemsetAsync(scratch, 0, (kStaticHeaderWords + static_cast<size_t>(B)) * sizeof(uint32_t), stream) !=
-        cudaSuccess)
-        return BLINK_CUDA_ERROR;
     const int grid = (sum_k + kReadoutWarps - 1) / kReadoutWarps;
-    readout_kernel<true><<<grid, kReadoutWarps * 32, 0, stream>>>(hidden, hidden_row_stride, hidden_rows, d_last_idx,
-                                                           d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
-                                                           sum_k, kLog2e / temperature, d_probs, d_logits, nullptr,
-                                                           nullptr, counters, err);
+    const float log2e_over_t = kLog2e / temperature;
+    // Calls share the array: clear this call's error word (and its tickets) first.  Large label
+    // counts take the same two-launch form as blink_label_readout, which uses no tickets.
+    const bool split = sum_k >= kSplitFinishLabels;
+    const size_t clear_words = kStaticHeaderWords + (split ? 0 : static_cast<size_t>(B));
+    if (cudaMemsetAsync(scratch, 0, clear_words * sizeof(uint32_t), stream) != cudaSuccess) return BLINK_CUDA_ERROR;
+    if (split) {
+        readout_kernel<false><<<grid, kReadoutWarps * 32, 0, stream>>>(
+            hidden, hidden_row_stride, hidden_rows, d_last_idx, d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
+            sum_k, log2e_over_t, d_probs, d_logits, nullptr, nullptr, counters, err);
+        if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+        readout_finish_kernel<<<(B + kReadoutWarps - 1) / kReadoutWarps, kReadoutWarps * 32, 0, stream>>>(
+            d_label_off, B, sum_k, log2e_over_t, d_probs, nullptr, nullptr, err);
+    } else {
+        readout_kernel<true><<<grid, kReadoutWarps * 32, 0, stream>>>(
+            hidden, hidden_row_stride, hidden_rows, d_last_idx, d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
+            sum_k, log2e_over_t, d_probs, d_logits, nullptr, nullptr, counters, err);
+    }
     if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
     if (h_probs) {
         int32_t word = 0;

@@ -31,6 +31,18 @@ def test_header_declares_the_three_path_calls():
         assert n in names
 
 
+def test_boundary_names_of_the_scope_table(lib):
+    """The boundary's calls by name: the status string, the three path calls and the workspace
+    query of each that takes a workspace (the planner's returns 0: its scratch is its outputs)."""
+    raw = ctypes.CDLL(blink.LIB_PATH)
+    for n in ("blink_status_string", "blink_pack_plan_workspace", "blink_pack_plan", "blink_attention_workspace",
+              "blink_prefix_tail_attention", "blink_label_readout_workspace", "blink_label_readout"):
+        assert n in _declared(), n
+        assert hasattr(raw, n), n
+    for n in (1, 2048, 2049, 32768):
+        assert blink.pack_plan_workspace_bytes(n) == 0
+
+
 def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(blink.LIB_PATH)
     for name in _declared():
