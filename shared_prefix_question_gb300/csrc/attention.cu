@@ -941,57 +941,61 @@ __global__ void __launch_bounds__(kThreads1, 2)
     if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols1);
 }
 
-// Merge of the prefix chunks (one request): block (u, q) with u = row pair * Hkv + kv head takes
-// output columns [32 q, 32 q + 32); thread = row of the pair's two M tiles.  O = sum_c w_c O_c /
-// sum_c w_c with w_c = exp(lse_c - max_c lse_c); the LSE (written by the q = 0 blocks) is
-// max + log(sum w).  Runs after the attention launch (stream order), so every partial is
-// complete.
+// Merge of the prefix chunks (one request).  Thread = (row of a row pair's two M tiles, 8
+// output columns); a block covers 16 rows of one unit (u = row pair * Hkv + kv head), the 16
+// threads of a row reading its partials as one contiguous run.  O = sum_c w_c O_c / sum_c w_c
+// with w_c = exp(lse_c - max_c lse_c); the LSE (written by each row's first thread) is
+// max + log(sum w).  Every chunk's loads of a row are independent, so a thread has them all in
+// flight at once.  Runs after the attention launch (stream order): every partial is complete.
+constexpr int kMergeRows = 16;  // rows per merge block
+
 template <int D>
-__global__ void __launch_bounds__(2 * BM)
+__global__ void __launch_bounds__(kMergeRows * (D / 8))
     split_merge_kernel(const AttnArgs a, int nb)
 {
-    const int unit = blockIdx.x;
-    const int q = blockIdx.y;
+    constexpr int kGroups = D / 8;
+    const int unit = blockIdx.x / (2 * BM / kMergeRows);
+    const int rr = (blockIdx.x % (2 * BM / kMergeRows)) * kMergeRows + threadIdx.x / kGroups;  // row of the pair
+    const int cg = threadIdx.x % kGroups;
     const int bx = unit / a.Hkv, head = unit % a.Hkv;
-    const int t = threadIdx.x / BM, r = threadIdx.x % BM;
+    const int t = rr / BM, r = rr % BM;
     const int t0 = (nb - 1 - bx) * 2 * a.tpt;
     const int tok = t0 + t * a.tpt + r / a.g;
     const int hq = head * a.g + r % a.g;
     if (r >= a.g * a.tpt || tok >= a.rows) return;
-    const int64_t row0 = static_cast<int64_t>(unit) * a.n_split * (2 * BM) + threadIdx.x;
+    const int S = a.n_split;
+    const int64_t row0 = static_cast<int64_t>(unit) * S * (2 * BM) + rr;
     float mx = -INFINITY;
-    for (int c = 0; c < a.n_split; ++c) mx = fmaxf(mx, __ldg(a.part_lse + row0 + c * (2 * BM)));
+    for (int c = 0; c < S; ++c) mx = fmaxf(mx, __ldg(a.part_lse + row0 + c * (2 * BM)));
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
     float wsum = 0.f;
-    if (mx != -INFINITY)
-        for (int c = 0; c < a.n_split; ++c) wsum += ptx::ex2((__ldg(a.part_lse + row0 + c * (2 * BM)) - mx) * kLog2e);
-    const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
-    uint16_t *dst = a.out + (static_cast<int64_t>(tok) * a.Hq + hq) * D;
-    {
-        float acc[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-        for (int c = 0; c < a.n_split && mx != -INFINITY; ++c) {
+    if (mx != -INFINITY) {
+#pragma unroll 2
+        for (int c = 0; c < S; ++c) {
             const float lc = __ldg(a.part_lse + row0 + c * (2 * BM));
-            if (lc == -INFINITY) continue;
-            const float w = ptx::ex2((lc - mx) * kLog2e);
-            const float4 *p4 = reinterpret_cast<const float4 *>(a.part_o + (row0 + c * (2 * BM)) * D + q * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 v = __ldg(p4 + j);
-                acc[4 * j] = fmaf(w, v.x, acc[4 * j]);
-                acc[4 * j + 1] = fmaf(w, v.y, acc[4 * j + 1]);
-                acc[4 * j + 2] = fmaf(w, v.z, acc[4 * j + 2]);
-                acc[4 * j + 3] = fmaf(w, v.w, acc[4 * j + 3]);
-            }
+            const float w = lc == -INFINITY ? 0.f : ptx::ex2((lc - mx) * kLog2e);
+            const float4 *p4 = reinterpret_cast<const float4 *>(a.part_o + (row0 + c * (2 * BM)) * D + cg * 8);
+            const float4 v0 = __ldg(p4), v1 = __ldg(p4 + 1);
+            wsum += w;
+            acc[0] = fmaf(w, v0.x, acc[0]);
+            acc[1] = fmaf(w, v0.y, acc[1]);
+            acc[2] = fmaf(w, v0.z, acc[2]);
+            acc[3] = fmaf(w, v0.w, acc[3]);
+            acc[4] = fmaf(w, v1.x, acc[4]);
+            acc[5] = fmaf(w, v1.y, acc[5]);
+            acc[6] = fmaf(w, v1.z, acc[6]);
+            acc[7] = fmaf(w, v1.w, acc[7]);
         }
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) pk[j] = ptx::pack_bf16x2(acc[2 * j] * inv, acc[2 * j + 1] * inv);
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst + q * 32);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
     }
-    if (a.lse && q == 0) a.lse[static_cast<int64_t>(hq) * a.rows + tok] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+    const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+    uint16_t *dst = a.out + (static_cast<int64_t>(tok) * a.Hq + hq) * D + cg * 8;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                 ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                                                 ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv),
+                                                 ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv));
+    if (a.lse && cg == 0) a.lse[static_cast<int64_t>(hq) * a.rows + tok] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
 }
 
 }  // namespace
@@ -1223,10 +1227,11 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
     if (a.n_split > 1) {
         if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
         const unsigned units = static_cast<unsigned>(blocks * Hkv);
+        const unsigned mblocks = units * (2 * BM / kMergeRows);
         if (d == 128)
-            split_merge_kernel<128><<<dim3(units, 128 / 32), 2 * BM, 0, stream>>>(a, static_cast<int>(blocks));
+            split_merge_kernel<128><<<mblocks, kMergeRows * (128 / 8), 0, stream>>>(a, static_cast<int>(blocks));
         else
-            split_merge_kernel<64><<<dim3(units, 64 / 32), 2 * BM, 0, stream>>>(a, static_cast<int>(blocks));
+            split_merge_kernel<64><<<mblocks, kMergeRows * (64 / 8), 0, stream>>>(a, static_cast<int>(blocks));
     }
     if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
     return BLINK_OK;
