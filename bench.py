@@ -30,6 +30,10 @@ if ROOT not in sys.path:
 
 METRIC = "questions/sec and prefill tokens/sec at 1 GB300; % BF16 TC peak and % HBM BW"
 FLUSH_BYTES = 512 << 20  # flushed between timed steps: larger than the 129 MB L2
+# Spec-sheet figures of the part, reported beside the fractions of the measured peaks (the
+# measured copy bandwidth and bf16 GEMM rate are the roofline denominators).
+SPEC_TFLOPS = 2500.0  # dense bf16, TFLOP/s
+SPEC_GBS = 8000.0     # HBM3e, GB/s
 
 
 def flush_l2(buf):
@@ -439,6 +443,7 @@ def main():
                              f"attention_{w.name}")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                 "frac": achieved / tc_peak, "traffic": traffic,
+                "spec_peak": SPEC_TFLOPS, "frac_spec": achieved / SPEC_TFLOPS,
                 "kernel": "attention_kernel<128>", "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)",
                 "flops_per_launch": flops}
 
@@ -536,11 +541,13 @@ def attention_config_row(blink, dev, name, tc_peak, hbm_peak, flush, lengths=Non
     ms = statistics.mean(ms_all)
     fl = attention_flops(lengths, w.P, w.Hq, w.d)
     row = {"ms": ms, **spread(ms_all), "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / tc_peak,
+           "frac_spec": fl / ms / 1e9 / SPEC_TFLOPS,
            "shape": w.description if len(lengths) == w.n else f"{len(lengths)} question(s), tails {list(lengths)}, "
                                                                  f"prefix {w.P}, {w.Hq}/{w.Hkv} heads"}
     if not w.P:
         nbytes = rows * (2 * w.Hq + 2 * w.Hkv) * w.d * 2
-        row.update({"bytes": nbytes, "GBs": nbytes / ms / 1e6, "byte_frac": nbytes / ms / 1e6 / hbm_peak})
+        row.update({"bytes": nbytes, "GBs": nbytes / ms / 1e6, "byte_frac": nbytes / ms / 1e6 / hbm_peak,
+                    "byte_frac_spec": nbytes / ms / 1e6 / SPEC_GBS})
     return row
 
 
@@ -573,6 +580,7 @@ def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
                flush)
     fl = attention_flops(np.array([P]), 0, Hq, d)
     out["prefix_self_attention"] = {"ms": ms, "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / tc_peak,
+                                    "frac_spec": fl / ms / 1e9 / SPEC_TFLOPS,
                                     "shape": f"one causal sequence of {P} tokens, {Hq}/{Hkv} heads, d {d}"}
     # 2. the prefix K/V rows written into an arena region
     slots = P + 4096
@@ -581,6 +589,7 @@ def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
     ms = _time(lambda: blink.blink_kv_to_arena(k, v, ak, av, 1024), flush)
     nbytes = 2 * 2 * P * Hkv * d * 2
     out["kv_to_arena"] = {"ms": ms, "GBs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_peak,
+                          "frac_spec": nbytes / ms / 1e6 / SPEC_GBS,
                           "bytes": nbytes, "shape": f"{P} rows of K and V ({Hkv}x{d} bf16) read and written"}
     del q, o
     # 3. shared-prefix length over the questions' full prompts (prefix + tail each)
@@ -616,6 +625,7 @@ def other_rows(blink, dev, w, ins, flush, hbm_peak, tc_peak, peak_kind):
         flush)
     fl = sum(attention_flops(t, Pr, Hq, d) for t in tails)
     out["several_requests"] = {"ms": ms, "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / tc_peak,
+                               "frac_spec": fl / ms / 1e9 / SPEC_TFLOPS,
                                "shape": f"{n_req} requests x (prefix {Pr}, 16 tails U[32,128]) in one launch"}
     # 5. the pack plan at its largest size: 64 requests x 512 questions (32768 lengths U[16,1024])
     out["pack_plan_32768"] = pack_plan_row(blink, dev, flush)
@@ -689,6 +699,7 @@ def readout_stress(blink, dev, hbm_peak, peak_kind, flush, args):
     achieved = nbytes / (ms / 1000.0) / 1e9
     del W
     return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+            "spec_peak": SPEC_GBS, "frac_spec": achieved / SPEC_GBS,
             "traffic": traffic_record(os.path.join(ROOT, "shared_prefix_question_gb300", "csrc", "readout.cu"),
                                       "readout_stress"),
             "kernel": "readout_kernel", "ms": ms, "algorithmic_bytes": nbytes,
