@@ -72,7 +72,8 @@ struct AttnArgs {
     // its own sum) and LSE, the last chunk also runs the tail tiles, and split_merge_kernel then
     // merges the chunks of every row by LSE.
     int n_split, split_tiles;
-    float *part_o;    // [units][n_split][2 BM][D], unit = row pair * Hkv + kv head
+    float *part_o;    // [units][n_split][D / 4][2 BM] float4, unit = row pair * Hkv + kv head (a column
+                      // group's rows contiguous, so a warp's partial stores are coalesced)
     float *part_lse;  // [units][n_split][2 BM]
     int n_req;
     int req_row[kMaxRequests + 1];
@@ -572,11 +573,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 32; ++j) o[j] = 0u;
                 }
                 if (row_ok && partial) {
-                    float4 *p4 = reinterpret_cast<float4 *>(a.part_o + prow * D + c * 32);
+                    // float4 group g of this row at [unit, chunk, g, row]
+                    float4 *p4 = reinterpret_cast<float4 *>(a.part_o) +
+                                 ((prow - (t * BM + r)) / (2 * BM) * (D / 4) + c * 8) * (2 * BM) + t * BM + r;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        p4[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                                            __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+                        p4[j * (2 * BM)] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                                       __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
                 } else if (row_ok) {
                     uint32_t pk[16];
 #pragma unroll
@@ -942,9 +945,10 @@ __global__ void __launch_bounds__(kThreads1, 2)
 }
 
 // Merge of the prefix chunks (one request).  Thread = (row of a row pair's two M tiles, 8
-// output columns); a block covers 16 rows of one unit (u = row pair * Hkv + kv head), the 16
-// threads of a row reading its partials as one contiguous run.  O = sum_c w_c O_c / sum_c w_c
-// with w_c = exp(lse_c - max_c lse_c); the LSE (written by each row's first thread) is
+// output columns); a block covers 16 rows of one unit (u = row pair * Hkv + kv head) and the
+// 16 threads of one column group take consecutive rows, reading the partials (stored column
+// group by column group) as contiguous runs.  O = sum_c w_c O_c / sum_c w_c with
+// w_c = exp(lse_c - max_c lse_c); the LSE (written by each row's first column group) is
 // max + log(sum w).  Every chunk's loads of a row are independent, so a thread has them all in
 // flight at once.  Runs after the attention launch (stream order): every partial is complete.
 constexpr int kMergeRows = 16;  // rows per merge block
@@ -953,10 +957,9 @@ template <int D>
 __global__ void __launch_bounds__(kMergeRows * (D / 8))
     split_merge_kernel(const AttnArgs a, int nb)
 {
-    constexpr int kGroups = D / 8;
     const int unit = blockIdx.x / (2 * BM / kMergeRows);
-    const int rr = (blockIdx.x % (2 * BM / kMergeRows)) * kMergeRows + threadIdx.x / kGroups;  // row of the pair
-    const int cg = threadIdx.x % kGroups;
+    const int rr = (blockIdx.x % (2 * BM / kMergeRows)) * kMergeRows + threadIdx.x % kMergeRows;  // row of the pair
+    const int cg = threadIdx.x / kMergeRows;
     const int bx = unit / a.Hkv, head = unit % a.Hkv;
     const int t = rr / BM, r = rr % BM;
     const int t0 = (nb - 1 - bx) * 2 * a.tpt;
@@ -976,8 +979,9 @@ __global__ void __launch_bounds__(kMergeRows * (D / 8))
         for (int c = 0; c < S; ++c) {
             const float lc = __ldg(a.part_lse + row0 + c * (2 * BM));
             const float w = lc == -INFINITY ? 0.f : ptx::ex2((lc - mx) * kLog2e);
-            const float4 *p4 = reinterpret_cast<const float4 *>(a.part_o + (row0 + c * (2 * BM)) * D + cg * 8);
-            const float4 v0 = __ldg(p4), v1 = __ldg(p4 + 1);
+            const float4 *p4 = reinterpret_cast<const float4 *>(a.part_o) +
+                               ((static_cast<int64_t>(unit) * S + c) * (D / 4) + 2 * cg) * (2 * BM) + rr;
+            const float4 v0 = __ldg(p4), v1 = __ldg(p4 + 2 * BM);
             wsum += w;
             acc[0] = fmaf(w, v0.x, acc[0]);
             acc[1] = fmaf(w, v0.y, acc[1]);
