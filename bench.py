@@ -2,8 +2,9 @@
 """Benchmark of the shared-prefix one-pass decision hot path on GB300.
 
 One step = one pass of the whole path over one batch: the token-budget pack plan, the
-prefix-tail attention of every question's tail against the shared prefix (one attention layer)
-and the label readout with its temperature softmax.  Default workload: the long-document case
+prefix-tail attention of every question's tail against the shared prefix (one attention layer),
+the label readout with its temperature softmax and typed answers, and the forward's one host
+transfer of the probabilities and answers.  Default workload: the long-document case
 (prefix 18432 tokens, 64 questions with tails U[64,256], 32/8 heads, d 128, hidden 2560,
 vocabulary 151936, 2-26 labels, T 0.7), synthetic and seeded.
 
@@ -382,6 +383,11 @@ def main():
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    # the forward's one host transfer: probabilities and answers into pinned host memory (issued
+    # on the stream without a host wait, as a server overlapping forwards would)
+    h_probs = torch.empty(sum_k, dtype=torch.float32, pin_memory=True)
+    h_answers = torch.empty(n, 3, dtype=torch.float32, pin_memory=True)
+
     def step(ev=None):
         if ev:
             ev[0].record(stream)
@@ -396,6 +402,10 @@ def main():
                                   slot_of=plan["slot_of"], qtype=qtype, answers=answers)
         if ev:
             ev[3].record(stream)
+        h_probs.copy_(probs, non_blocking=True)
+        h_answers.copy_(answers, non_blocking=True)
+        if ev:
+            ev[4].record(stream)
 
     for _ in range(args.warmup):
         flush_l2(flush)
@@ -411,7 +421,7 @@ def main():
     sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
     if rank == 0:
         sampler.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -425,7 +435,8 @@ def main():
     plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     read_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    d2h_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -458,7 +469,7 @@ def main():
             "prefill_tokens_per_s": world * prefill_tokens / (ms_per_step / 1000.0),
             "tail_tokens_per_s": world * int(lengths.sum()) / (ms_per_step / 1000.0),
             "kernels_ms": {"plan": statistics.mean(plan_ms), "attention": attn_mean,
-                           "readout": statistics.mean(read_ms)},
+                           "readout": statistics.mean(read_ms), "d2h_probs_answers": statistics.mean(d2h_ms)},
             "spread_ms": {"step": spread(step_ms), "attention": spread(attn_ms)},
             "roofline": roofline, "gpu_launches": 3 * args.steps, "clocks": clocks}
 

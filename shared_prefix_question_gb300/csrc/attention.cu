@@ -72,9 +72,12 @@ struct AttnArgs {
     // its own sum) and LSE, the last chunk also runs the tail tiles, and split_merge_kernel then
     // merges the chunks of every row by LSE.
     int n_split, split_tiles;
-    float *part_o;    // [units][n_split][D / 4][2 BM] float4, unit = row pair * Hkv + kv head (a column
+    // Work units are (row pair, kv head), numbered kv-head-major: u = head * n_pairs + row pair.
+    // A launch runs units [unit0, unit0 + its grid / n_split).
+    int n_pairs, unit0;
+    float *part_o;    // [split units][n_split][D / 4][2 BM] float4, split unit = u - unit0 (a column
                       // group's rows contiguous, so a warp's partial stores are coalesced)
-    float *part_lse;  // [units][n_split][2 BM]
+    float *part_lse;  // [split units][n_split][2 BM]
     int n_req;
     int req_row[kMaxRequests + 1];
     int req_blk[kMaxRequests + 1];
@@ -178,9 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int head = blockIdx.y;
+    const int local = kSplit ? static_cast<int>(blockIdx.x) / a.n_split : static_cast<int>(blockIdx.x);
     const int split = kSplit ? static_cast<int>(blockIdx.x) % a.n_split : 0;  // prefix chunk
-    const int bx = kSplit ? static_cast<int>(blockIdx.x) / a.n_split : static_cast<int>(blockIdx.x);  // row pair
+    const int unit = a.unit0 + local;
+    const int head = unit / a.n_pairs;
+    const int bx = unit - head * a.n_pairs;  // row pair
     int req = 0;  // this block's request
     while (req + 1 < a.n_req && a.req_blk[req + 1] <= bx) ++req;
     const int req_begin = a.req_row[req], req_end = a.req_row[req + 1];
@@ -560,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float row_lse =
                 (owned && l > 0.f) ? (((m == -INFINITY) ? 0.f : m) + __log2f(l)) * kLn2 : -INFINITY;
             constexpr bool partial = kSplit;
-            const int64_t prow = ((static_cast<int64_t>(bx) * a.Hkv + head) * a.n_split + split) * (2 * BM) + t * BM + r;
+            const int64_t prow = (static_cast<int64_t>(local) * a.n_split + split) * (2 * BM) + t * BM + r;
             uint16_t *dst = a.out + (static_cast<int64_t>(tok) * a.Hq + hq) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -957,17 +962,18 @@ template <int D>
 __global__ void __launch_bounds__(kMergeRows * (D / 8))
     split_merge_kernel(const AttnArgs a, int nb)
 {
-    const int unit = blockIdx.x / (2 * BM / kMergeRows);
+    const int local = blockIdx.x / (2 * BM / kMergeRows);  // split unit
     const int rr = (blockIdx.x % (2 * BM / kMergeRows)) * kMergeRows + threadIdx.x % kMergeRows;  // row of the pair
     const int cg = threadIdx.x / kMergeRows;
-    const int bx = unit / a.Hkv, head = unit % a.Hkv;
+    const int unit = a.unit0 + local;
+    const int head = unit / a.n_pairs, bx = unit - head * a.n_pairs;
     const int t = rr / BM, r = rr % BM;
     const int t0 = (nb - 1 - bx) * 2 * a.tpt;
     const int tok = t0 + t * a.tpt + r / a.g;
     const int hq = head * a.g + r % a.g;
     if (r >= a.g * a.tpt || tok >= a.rows) return;
     const int S = a.n_split;
-    const int64_t row0 = static_cast<int64_t>(unit) * S * (2 * BM) + rr;
+    const int64_t row0 = static_cast<int64_t>(local) * S * (2 * BM) + rr;
     float mx = -INFINITY;
     for (int c = 0; c < S; ++c) mx = fmaxf(mx, __ldg(a.part_lse + row0 + c * (2 * BM)));
     float acc[8];
@@ -980,7 +986,7 @@ __global__ void __launch_bounds__(kMergeRows * (D / 8))
             const float lc = __ldg(a.part_lse + row0 + c * (2 * BM));
             const float w = lc == -INFINITY ? 0.f : ptx::ex2((lc - mx) * kLog2e);
             const float4 *p4 = reinterpret_cast<const float4 *>(a.part_o) +
-                               ((static_cast<int64_t>(unit) * S + c) * (D / 4) + 2 * cg) * (2 * BM) + rr;
+                               ((static_cast<int64_t>(local) * S + c) * (D / 4) + 2 * cg) * (2 * BM) + rr;
             const float4 v0 = __ldg(p4), v1 = __ldg(p4 + 2 * BM);
             wsum += w;
             acc[0] = fmaf(w, v0.x, acc[0]);
@@ -1023,41 +1029,62 @@ bool use_single_tile(const AttnArgs &a, int max_tail)
     return n_pre + (max_tail / 2 + BN - 1) / BN <= 8;
 }
 
-// Prefix chunks for a grid that leaves SMs idle (one request with a prefix).  Launch time is
-// modelled in KV-tile iterations: waves(units * S) * (chunk tiles + kFixedTiles), plus for S > 1
-// the merge launch and the fp32 partials written and read back (bytes / kBytesPerTile), where a
-// wave is one block per SM.  S >= 2 chunks of c >= kMinSplitTiles tiles are used when that beats
-// the unsplit launch by at least 10 % and the split grid stays within four waves.  S = 1
-// otherwise.  (Measured: one question against an 18k prefix runs 4x faster in 18 chunks; the 2k
-// workload, two waves of 160 blocks, runs 23 % slower in 2 chunks, which the model rejects.)
-void choose_split(int64_t units, int n_pre, int d, int sms, int &S, int &c)
+// Prefix chunks (one request with a prefix).  Launch time is modelled in KV-tile iterations:
+// waves(blocks) * (tiles a block runs + kFixedTiles), where a wave is one block per SM, plus,
+// when anything is split, the merge launch and the fp32 partials written and read back
+// (bytes / kBytesPerTile).  Two forms are weighed against the unsplit launch:
+//   - every unit cut into S >= 2 chunks of c >= kMinSplitTiles tiles, within four waves (a small
+//     grid: one question against a long prefix);
+//   - whole waves of units unsplit, and only the units of the last, partial wave cut into S
+//     chunks (c >= 1 tile) that run as one more wave (e.g. 160 row-pair units on 152 SMs: 152 run
+//     whole, the other 8 in 16 one-tile chunks, instead of a second wave of 8 whole units).
+// A split is used when it beats the unsplit launch by at least 10 %.  (Measured: one question
+// against an 18k prefix 4x faster in 9 chunks; every unit of the 2k workload cut in 2-4 chunks
+// 5-40 % slower, which the model rejects.)
+struct SplitPlan {
+    int64_t unit0;  // units [0, unit0) run whole; units [unit0, units) run in S chunks
+    int S, c;       // chunks per split unit and prefix tiles per chunk; S = 1: nothing split
+};
+
+SplitPlan choose_split(int64_t units, int n_pre, int d, int sms)
 {
-    constexpr int64_t kFixedTiles = 4;             // block start, pipeline fill and epilogue
-    constexpr int64_t kMergeTiles = 2;             // the merge launch
-    constexpr int64_t kBytesPerTile = 9ll << 20;   // DRAM bytes moved in one iteration's time
-    S = 1;
-    c = 1 << 30;
-    if (units < 1 || sms < 1 || n_pre < 2 * kMinSplitTiles) return;
+    constexpr int64_t kFixedTiles = 4;            // block start, pipeline fill and epilogue
+    constexpr int64_t kMergeTiles = 2;            // the merge launch
+    constexpr int64_t kBytesPerTile = 9ll << 20;  // DRAM bytes moved in one iteration's time
+    SplitPlan plan{units, 1, 1 << 30};
+    if (units < 1 || sms < 1 || n_pre < 2) return plan;
     auto waves = [&](int64_t u) { return (u + sms - 1) / sms; };
-    const int64_t unsplit = waves(units) * (n_pre + kFixedTiles);
-    int64_t best = unsplit * 9 / 10;  // a split has to win by 10 %
-    for (int s = 2; s <= n_pre / kMinSplitTiles; ++s) {
+    auto partial_cost = [&](int64_t split_blocks) {  // fp32 O written and read back
+        return kMergeTiles + split_blocks * (2 * BM) * d * 8 / kBytesPerTile;
+    };
+    int64_t best = waves(units) * (n_pre + kFixedTiles) * 9 / 10;  // a split has to win by 10 %
+    for (int s = 2; n_pre >= 2 * kMinSplitTiles && s <= n_pre / kMinSplitTiles; ++s) {
         const int cc = (n_pre + s - 1) / s;
         const int ss = (n_pre + cc - 1) / cc;
         if (ss < 2 || ss != s) continue;  // each chunk count considered once, at its own size
         if (units * ss > 4LL * sms) break;
-        const int64_t partial_bytes = units * ss * (2 * BM) * d * 8;  // fp32 O written and read
-        const int64_t cost = waves(units * ss) * (cc + kFixedTiles) + kMergeTiles + partial_bytes / kBytesPerTile;
+        const int64_t cost = waves(units * ss) * (cc + kFixedTiles) + partial_cost(units * ss);
         if (cost < best) {
             best = cost;
-            S = ss;
-            c = cc;
+            plan = SplitPlan{0, ss, cc};
         }
     }
+    const int64_t full = units / sms * sms, rest = units - full;
+    for (int s = 2; full > 0 && rest > 0 && s <= n_pre && rest * s <= sms; ++s) {
+        const int cc = (n_pre + s - 1) / s;
+        const int ss = (n_pre + cc - 1) / cc;
+        if (ss != s) continue;
+        const int64_t cost = full / sms * (n_pre + kFixedTiles) + (cc + kFixedTiles) + partial_cost(rest * ss);
+        if (cost < best) {
+            best = cost;
+            plan = SplitPlan{full, ss, cc};
+        }
+    }
+    return plan;
 }
 
-// Workspace after the 256-byte header when the prefix is split: partial LSE [units][S][2 BM]
-// and partial O [units][S][2 BM][d] (fp32), each region 256-byte aligned.
+// Workspace after the 256-byte header when the prefix is split: partial LSE [split units][S][2 BM]
+// and partial O [split units][S][d / 4][2 BM] (fp32), each region 256-byte aligned.
 struct SplitLayout {
     size_t lse, o, total;
 };
@@ -1164,26 +1191,31 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
     a.scale_log2 = sc * kLog2e;
 
-    // A small grid over one request's prefix: split the prefix (if the workspace has the room).
+    // One request's prefix: split it, for a small grid or for the last partial wave of units (if
+    // the workspace has the room).
     a.n_split = 1;
     a.split_tiles = 1 << 30;
     a.part_o = nullptr;
     a.part_lse = nullptr;
+    a.n_pairs = static_cast<int>(blocks);
+    a.unit0 = 0;
+    const int64_t units = blocks * Hkv;
+    int64_t whole_units = units;  // units run unsplit
     if (a.n_req == 1 && a.req_P[0] > 0) {
-        int S = 1, c = 1 << 30;
-        choose_split(blocks * Hkv, (a.req_P[0] + BN - 1) / BN, d, sm_count_attention(), S, c);
-        if (S > 1) {
-            const SplitLayout lay = split_layout(blocks * Hkv, S, d);
+        const SplitPlan plan = choose_split(units, (a.req_P[0] + BN - 1) / BN, d, sm_count_attention());
+        if (plan.S > 1) {
+            const SplitLayout lay = split_layout(units - plan.unit0, plan.S, d);
             if (ws_bytes >= lay.total) {
                 auto *wsb = static_cast<uint8_t *>(d_ws);
-                a.n_split = S;
-                a.split_tiles = c;
+                a.n_split = plan.S;
+                a.split_tiles = plan.c;
                 a.part_lse = reinterpret_cast<float *>(wsb + lay.lse);
                 a.part_o = reinterpret_cast<float *>(wsb + lay.o);
+                whole_units = plan.unit0;
             }
         }
     }
-    if (blocks * a.n_split > 0x7FFFFFFF) return BLINK_OUT_OF_RANGE;
+    if (units * a.n_split > 0x7FFFFFFF) return BLINK_OUT_OF_RANGE;
     // Unsplit launches of short work run the single-tile kernel (two blocks per SM).
     const bool single = a.n_split == 1 && use_single_tile(a, max_tail);
     if (single) {
@@ -1212,26 +1244,31 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
         if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
         return BLINK_OK;
     }
-    dim3 grid(static_cast<unsigned>(blocks * a.n_split), static_cast<unsigned>(Hkv));
-    if (d == 128) {
-        const int smem = Layout<128>::kAlloc;
-        auto kern = a.n_split > 1 ? attention_kernel<128, true> : attention_kernel<128, false>;
+    // Whole units first (one block each), then the split units (n_split blocks each) and their
+    // merge.  Each block takes all 512 tensor-memory columns, so one block fits per SM (for d = 64
+    // enough shared memory is reserved to keep it so).
+    const int smem = d == 128 ? Layout<128>::kAlloc : (Layout<64>::kAlloc > 120 * 1024 ? Layout<64>::kAlloc : 120 * 1024);
+    if (whole_units > 0) {
+        auto kern = d == 128 ? attention_kernel<128, false> : attention_kernel<64, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return BLINK_CUDA_ERROR;
-        kern<<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
-    } else {
-        // Reserve enough shared memory that only one block fits per SM: each block takes all
-        // 512 tensor-memory columns.
-        const int smem = Layout<64>::kAlloc > 120 * 1024 ? Layout<64>::kAlloc : 120 * 1024;
-        auto kern = a.n_split > 1 ? attention_kernel<64, true> : attention_kernel<64, false>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return BLINK_CUDA_ERROR;
-        kern<<<grid, kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
+        AttnArgs aw = a;
+        aw.n_split = 1;
+        aw.split_tiles = 1 << 30;
+        kern<<<static_cast<unsigned>(whole_units), kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail,
+                                                                            tm_vtail, aw);
+        if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
     }
     if (a.n_split > 1) {
+        a.unit0 = static_cast<int>(whole_units);
+        const int64_t split_units = units - whole_units;
+        auto kern = d == 128 ? attention_kernel<128, true> : attention_kernel<64, true>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return BLINK_CUDA_ERROR;
+        kern<<<static_cast<unsigned>(split_units * a.n_split), kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre,
+                                                                                        tm_ktail, tm_vtail, a);
         if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
-        const unsigned units = static_cast<unsigned>(blocks * Hkv);
-        const unsigned mblocks = units * (2 * BM / kMergeRows);
+        const unsigned mblocks = static_cast<unsigned>(split_units * (2 * BM / kMergeRows));
         if (d == 128)
             split_merge_kernel<128><<<mblocks, kMergeRows * (128 / 8), 0, stream>>>(a, static_cast<int>(blocks));
         else
@@ -1252,9 +1289,8 @@ extern "C" size_t blink_attention_workspace(int32_t rows, int32_t B, int32_t P, 
         return kHeaderBytes;
     const int tpt = BM / (Hq / Hkv);
     const int64_t blocks = ((static_cast<int64_t>(rows) + tpt - 1) / tpt + 1) / 2;
-    int S = 1, c = 1 << 30;
-    choose_split(blocks * Hkv, (P + BN - 1) / BN, d, sm_count_attention(), S, c);
-    return S > 1 ? split_layout(blocks * Hkv, S, d).total : kHeaderBytes;
+    const SplitPlan plan = choose_split(blocks * Hkv, (P + BN - 1) / BN, d, sm_count_attention());
+    return plan.S > 1 ? split_layout(blocks * Hkv - plan.unit0, plan.S, d).total : kHeaderBytes;
 }
 
 extern "C" blink_status blink_prefix_tail_attention(const blink_bf16 *q, const blink_bf16 *k_pre,

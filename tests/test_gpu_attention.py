@@ -243,11 +243,12 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
 @pytest.mark.parametrize("case", [
     # name, P, n tails, Hq, Hkv, padded width (0: varlen)
     ("g2", 3072, 40, 16, 8, 0),
-    ("g5-padded", 2500, 61, 10, 2, 64),
+    ("g5-padded", 2500, 58, 10, 2, 64),
 ], ids=lambda c: c[0])
 def test_attention_two_tile_kernel_all_rows(case):
     """A prefix of 20-24 key tiles with short tails runs the two-tile kernel (a block's estimated
-    KV iterations exceed the single-tile limit) with enough blocks that the prefix is not split;
+    KV iterations exceed the single-tile limit) in one wave of at most 152 blocks (the prefix is not
+    split: enough blocks for a small-grid split not to pay, no partial second wave to split);
     every row matches the oracle.  Both cases end a kv head's blocks on a row pair whose second
     tile starts past the last row; g = 5 leaves 3 of every 128 tile rows unused; the padded case
     checks that rows no question owns stay zero with LSE -inf.  (The small cases above, with a
@@ -267,5 +268,38 @@ def test_attention_two_tile_kernel_all_rows(case):
         owned = np.zeros(ins.rows, dtype=bool)
         for s, L in zip(ins.seq_start, ins.seq_len):
             owned[s:s + L] = True
+        assert (out[~owned] == 0).all()
+        assert np.isneginf(lse[:, ~owned]).all()
+
+
+@pytest.mark.parametrize("case", [
+    # name, P, Hq, Hkv, d, padded width (0: varlen)
+    ("d128-g4", 1024, 32, 8, 128, 0),
+    ("d64-g5-padded", 1000, 10, 2, 64, 64),
+], ids=lambda c: c[0])
+def test_attention_split_of_the_last_partial_wave(case):
+    """A launch a few (row pair, kv head) units longer than the GPU has SMs (the 2k workload's
+    shape: 160 units on 152 SMs) runs whole waves unsplit and cuts only the last partial wave's
+    units into prefix chunks, merged by LSE.  Every row matches the oracle, whichever launch
+    computed it; rows owned by no question stay zero with LSE -inf."""
+    name, P, Hq, Hkv, d, width = case
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tpt = 128 // (Hq // Hkv)
+    pairs = -(-(sms + 8) // Hkv)                 # row pairs per kv head: units = sms + 8 or a few more
+    n = pairs * 2 * tpt // (width or 40)         # questions of about 40 tokens (or padded rows)
+    rng = np.random.default_rng(900 + d)
+    lengths = rng.integers(30, 51, size=n)
+    ins = wl.attention_inputs(_w("tail-wave-" + name, 800 + d, P, Hq, Hkv, d), lengths=lengths, P=P,
+                              padded_width=width or None)
+    units = ((ins.rows + tpt - 1) // tpt + 1) // 2 * Hkv
+    assert sms < units < 2 * sms
+    assert blink.attention_workspace_bytes(ins.rows, len(lengths), P, Hq, Hkv, d) > 256  # the split path
+    out, lse, st = run_attention(ins, padded=bool(width))
+    assert st == blink.BLINK_OK
+    compare_attention(ins, out, lse)
+    if width:
+        owned = np.zeros(ins.rows, dtype=bool)
+        for s0, L in zip(ins.seq_start, ins.seq_len):
+            owned[s0:s0 + L] = True
         assert (out[~owned] == 0).all()
         assert np.isneginf(lse[:, ~owned]).all()
