@@ -11,10 +11,8 @@ namespace blink {
 
 // Layout of the first 256 bytes of every workspace: the device error word, then reserved space.
 struct WorkspaceHeader {
-    int32_t error;       // 0 = fine, else a blink_status latched by a kernel
-    uint32_t work_next;  // persistent attention launches: next work item (0 between launches)
-    uint32_t work_done;  // persistent attention launches: blocks finished (0 between launches)
-    int32_t reserved[61];
+    int32_t error;      // 0 = fine, else a blink_status latched by a kernel
+    int32_t reserved[63];
 };
 static_assert(sizeof(WorkspaceHeader) == 256, "workspace header is 256 bytes");
 

@@ -115,15 +115,6 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
-// Prefetch of one tensor-map box into L2 (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t x, int32_t y, int32_t z)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // ---------------------------------------------------------------------------------------------
 // tcgen05: tensor memory allocation, MMA, commit, TMEM loads and stores
 // ---------------------------------------------------------------------------------------------
