@@ -931,9 +931,12 @@ __global__ void __launch_bounds__(kThreads1, 2)
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         pk[j] = ptx::pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    // 32-byte stores: a warp's 32 rows land in 32 places, so each store should at
+                    // least fill a whole DRAM sector (measured 3 % faster on short causal work; in
+                    // the two-tile kernel the extra registers cost spills and 1 %)
+                    uint16_t *d8 = dst + c * 32;
+                    ptx::st_global_v8(d8, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+                    ptx::st_global_v8(d8 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
                 }
             }
             if (row_ok && a.lse) {
