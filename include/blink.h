@@ -178,10 +178,13 @@ blink_status blink_kv_to_arena(const blink_bf16 *k_src, const blink_bf16 *v_src,
  * lse   [Hq, rows]       optional (may be NULL): fp32 natural-log log-sum-exp of each row
  * d_ws, ws_bytes         workspace of at least blink_attention_workspace(...) bytes, zero-filled
  *                        before its first use; the first word is the device error word
- * Small grids (one request whose (token-pair, kv head) blocks leave SMs idle, e.g. a few
- * questions against a long prefix): when a launch-time model predicts a clear gain, the prefix is
- * cut into chunks of at least 4 key tiles run by separate blocks, and their partial outputs are
- * merged by LSE in a second launch (the merge of the prefix and tail parts, applied again).  blink_attention_workspace then includes room for the fp32 partials (it sizes them for
+ * Prefix chunks (one request with a prefix; the work units are (row pair, kv head)): when a
+ * launch-time model predicts a clear gain, units run their prefix in chunks of key tiles on
+ * separate blocks whose partial outputs are merged by LSE in a further launch (the merge of the
+ * prefix and tail parts, applied again).  Either every unit is cut (a small grid, e.g. a few
+ * questions against a long prefix: chunks of at least 4 tiles), or whole waves of units run
+ * unsplit and only the units of the last, partial wave are cut, into chunks that fill one more
+ * wave.  blink_attention_workspace then includes room for the fp32 partials (it sizes them for
  * the current device); with a smaller workspace the call runs unsplit.  Results agree with the
  * unsplit path within the rounding of the merge.
  * Errors: BLINK_INVALID_ARG, BLINK_OUT_OF_RANGE, BLINK_WORKSPACE_TOO_SMALL, BLINK_CUDA_ERROR;
