@@ -24,11 +24,13 @@
 // tensor core runs the other tile's products.
 //
 // Small grids (one request whose blocks fill at most half of the SMs, e.g. one question against
-// a long prefix): the prefix tiles are cut into chunks, one block per (row pair, kv head, chunk);
-// each writes its partial O (normalised by its own sum) and LSE in fp32, the last chunk also runs
-// the tail tiles, and split_merge_kernel combines the chunks by LSE -- the same merge that joins
-// the prefix and tail parts.  The chunked form is a separate instantiation (kSplit), so the
-// common unsplit kernel carries none of it.
+// a long prefix) and the last partial wave of a launch: the prefix tiles of some units are cut
+// into chunks, one block per (row pair, kv head, chunk); each writes its partial O (normalised by
+// its own sum) and LSE in fp32, the last chunk also runs the tail tiles, and split_merge_kernel
+// combines the chunks by LSE -- the same merge that joins the prefix and tail parts.  The whole
+// units and the chunks run in one launch (whole units first, so a chunk starts on the first SM
+// that frees up); the chunked form is a separate instantiation (kSplit), so the common unsplit
+// kernel carries none of it.
 #include <cstdint>
 
 #include "common.cuh"
@@ -67,13 +69,15 @@ struct AttnArgs {
     // Requests: request r owns tail rows [req_row[r], req_row[r+1]) and the prefix of req_P[r]
     // tokens at arena slots [req_pre[r], req_pre[r] + req_P[r]).  Blocks [req_blk[r], req_blk[r+1])
     // work on request r (a block never straddles two requests).
-    // Split of the prefix (one request only): with n_split > 1 the prefix tiles are cut into
-    // chunks of split_tiles; unit (row pair, kv head, chunk) writes its partial O (normalised by
-    // its own sum) and LSE, the last chunk also runs the tail tiles, and split_merge_kernel then
-    // merges the chunks of every row by LSE.
+    // Split of the prefix (one request only): with n_split > 1 the prefix tiles of units
+    // [unit0, ...) are cut into chunks of split_tiles (the last chunk: the remaining 0 ..
+    // split_tiles tiles, plus the tail tiles); unit (row pair, kv head, chunk) writes its
+    // partial O (normalised by its own sum) and LSE, the last chunk also runs the tail tiles, and
+    // split_merge_kernel then merges the chunks of every row by LSE.
     int n_split, split_tiles;
     // Work units are (row pair, kv head), numbered kv-head-major: u = head * n_pairs + row pair.
-    // A launch runs units [unit0, unit0 + its grid / n_split).
+    // Block b < unit0 runs unit b whole; block unit0 + j * n_split + c runs chunk c of unit
+    // unit0 + j (the chunked instantiation only; the unsplit one runs unit b for every block b).
     int n_pairs, unit0;
     float *part_o;    // [split units][n_split][D / 4][2 BM] float4, split unit = u - unit0 (a column
                       // group's rows contiguous, so a warp's partial stores are coalesced)
@@ -153,8 +157,8 @@ __device__ __forceinline__ bool question_ok(const AttnArgs &a, int s, int L)
     return L >= 1 && L <= a.max_tail && s >= 0 && static_cast<long long>(s) + L <= a.rows;
 }
 
-// kSplit: this launch runs prefix chunks (n_split > 1) and writes partial results; without it
-// the chunk arithmetic folds away and the kernel is the plain one.
+// kSplit: this launch runs prefix chunks (n_split > 1) after its whole units and writes their
+// partial results; without it the chunk arithmetic folds away and the kernel is the plain one.
 template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kpre,
@@ -181,18 +185,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int local = kSplit ? static_cast<int>(blockIdx.x) / a.n_split : static_cast<int>(blockIdx.x);
-    const int split = kSplit ? static_cast<int>(blockIdx.x) % a.n_split : 0;  // prefix chunk
-    const int unit = a.unit0 + local;
+    const int bid = static_cast<int>(blockIdx.x);
+    const bool chunk = kSplit && bid >= a.unit0;                     // a prefix chunk, not a whole unit
+    const int local = chunk ? (bid - a.unit0) / a.n_split : 0;       // split unit
+    const int split = chunk ? (bid - a.unit0) % a.n_split : 0;       // prefix chunk
+    const int unit = chunk ? a.unit0 + local : bid;
     const int head = unit / a.n_pairs;
     const int bx = unit - head * a.n_pairs;  // row pair
     int req = 0;  // this block's request
     while (req + 1 < a.n_req && a.req_blk[req + 1] <= bx) ++req;
     const int req_begin = a.req_row[req], req_end = a.req_row[req + 1];
     const int P = a.req_P[req], pre_start = a.req_pre[req];
-    const int pre_lo = kSplit ? split * a.split_tiles : 0;  // first prefix tile of this unit
-    const int n_pre = kSplit ? max(0, min((P + BN - 1) / BN - pre_lo, a.split_tiles)) : (P + BN - 1) / BN;
-    const bool has_tail = !kSplit || split == a.n_split - 1;
+    const int pre_lo = chunk ? split * a.split_tiles : 0;  // first prefix tile of this unit
+    const int n_pre = chunk ? max(0, min((P + BN - 1) / BN - pre_lo, a.split_tiles)) : (P + BN - 1) / BN;
+    const bool has_tail = !chunk || split == a.n_split - 1;
+    const int n_early = min(n_pre, kSlots / 2);  // prefix iterations copied before the tail search
     // Within a request the blocks run from the last row pair to the first: with a causal tail the
     // late pairs have the most keys, and starting them first shortens the end of the launch.
     const int t0 = req_begin + (a.req_blk[req + 1] - 1 - bx) * 2 * a.tpt;
@@ -226,6 +233,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int p = 0; p < L::kPanels; ++p)
                     ptx::tma_load_3d((t == 0 ? q_s0 : q_s1) + p * kHalfBytes, &tm_q, p * 64, head * a.g,
                                      t0 + t * a.tpt, q_full);
+            // The first prefix tiles need no schedule either: their copies run during the search
+            // for the block's tail keys below (the ring's first slots are free).
+            for (int it = 0; it < n_early; ++it) {
+                uint64_t *stage_full = full + (it & 1);
+                const int kb = pre_start + (pre_lo + it) * BN;
+                for (int kv = 0; kv < 2; ++kv) {
+                    ptx::mbar_arrive_expect_tx(stage_full, L::kKVTileBytes);
+                    for (int p = 0; p < L::kPanels; ++p)
+                        ptx::tma_load_3d(kv_s + (2 * it + kv) * L::kKVTileBytes + p * kHalfBytes,
+                                         kv ? &tm_vpre : &tm_kpre, p * 64, head, kb, stage_full);
+                }
+            }
         }
         __syncwarp();
         // Tail keys this block needs: from the start of the first question it touches.
@@ -285,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // released on its own (K after S_1, V after the product P_1 V) so neither copy waits for
         // the other's use.
         if (lane == 0) {
-            int n = 0;
-            for (int it = 0; it < n_iter; ++it) {
+            int n = 2 * n_early;
+            for (int it = n_early; it < n_iter; ++it) {
                 const bool pre = it < n_pre;
                 const int kb = pre ? pre_start + (pre_lo + it) * BN : kbeg + (it - n_pre) * BN;
                 uint64_t *stage_full = full + (it & 1);
@@ -310,6 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
             }
+            // The merge of the chunks is this launch's programmatic dependent: let it be scheduled
+            // once every block is this close to its end (it waits for the grid's end to read).
+            if constexpr (kSplit) ptx::grid_launch_dependents();
             // Drain: every copy issued must have landed before the block may exit.  Copies of
             // iterations before the last two were waited for by the MMA thread before their slots
             // were reused.
@@ -564,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = (owned && l > 0.f) ? 1.0f / l : 0.f;
             const float row_lse =
                 (owned && l > 0.f) ? (((m == -INFINITY) ? 0.f : m) + __log2f(l)) * kLn2 : -INFINITY;
-            constexpr bool partial = kSplit;
+            const bool partial = chunk;
             const int64_t prow = (static_cast<int64_t>(local) * a.n_split + split) * (2 * BM) + t * BM + r;
             uint16_t *dst = a.out + (static_cast<int64_t>(tok) * a.Hq + hq) * D;
 #pragma unroll
@@ -957,14 +979,16 @@ __global__ void __launch_bounds__(kThreads1, 2)
 // 16 threads of one column group take consecutive rows, reading the partials (stored column
 // group by column group) as contiguous runs.  O = sum_c w_c O_c / sum_c w_c with
 // w_c = exp(lse_c - max_c lse_c); the LSE (written by each row's first column group) is
-// max + log(sum w).  Every chunk's loads of a row are independent, so a thread has them all in
-// flight at once.  Runs after the attention launch (stream order): every partial is complete.
+// max + log(sum w).  Launched as the attention launch's programmatic dependent, so its blocks may
+// be resident before that launch ends; each waits for the attention grid's end (and the
+// visibility of its partials) before it reads anything.
 constexpr int kMergeRows = 16;  // rows per merge block
 
 template <int D>
 __global__ void __launch_bounds__(kMergeRows * (D / 8))
     split_merge_kernel(const AttnArgs a, int nb)
 {
+    ptx::grid_dep_wait();  // every block, before any read or early return
     const int local = blockIdx.x / (2 * BM / kMergeRows);  // split unit
     const int rr = (blockIdx.x % (2 * BM / kMergeRows)) * kMergeRows + threadIdx.x % kMergeRows;  // row of the pair
     const int cg = threadIdx.x / kMergeRows;
@@ -977,29 +1001,51 @@ __global__ void __launch_bounds__(kMergeRows * (D / 8))
     if (r >= a.g * a.tpt || tok >= a.rows) return;
     const int S = a.n_split;
     const int64_t row0 = static_cast<int64_t>(local) * S * (2 * BM) + rr;
-    float mx = -INFINITY;
-    for (int c = 0; c < S; ++c) mx = fmaxf(mx, __ldg(a.part_lse + row0 + c * (2 * BM)));
-    float acc[8];
+    // One pass over the chunks in groups of eight: a group's LSE and O loads are all issued before
+    // any is used (one L2 round trip per group), and the running sums are rescaled to each new
+    // maximum, so the weights are exp(lse_c - max) with max over all chunks, as above.
+    constexpr int kGroup = 8;
+    float mx = -INFINITY, wsum = 0.f, acc[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-#pragma unroll 2
-        for (int c = 0; c < S; ++c) {
-            const float lc = __ldg(a.part_lse + row0 + c * (2 * BM));
-            const float w = lc == -INFINITY ? 0.f : ptx::ex2((lc - mx) * kLog2e);
-            const float4 *p4 = reinterpret_cast<const float4 *>(a.part_o) +
-                               ((static_cast<int64_t>(local) * S + c) * (D / 4) + 2 * cg) * (2 * BM) + rr;
-            const float4 v0 = __ldg(p4), v1 = __ldg(p4 + 2 * BM);
+    for (int c0 = 0; c0 < S; c0 += kGroup) {
+        float lc[kGroup];
+        float4 v0[kGroup], v1[kGroup];
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+            const int c = c0 + k;
+            if (c < S) {
+                lc[k] = __ldg(a.part_lse + row0 + c * (2 * BM));
+                const float4 *p4 = reinterpret_cast<const float4 *>(a.part_o) +
+                                   ((static_cast<int64_t>(local) * S + c) * (D / 4) + 2 * cg) * (2 * BM) + rr;
+                v0[k] = __ldg(p4);
+                v1[k] = __ldg(p4 + 2 * BM);
+            } else {
+                lc[k] = -INFINITY;
+                v0[k] = v1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float gm = mx;
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) gm = fmaxf(gm, lc[k]);
+        if (gm == -INFINITY) continue;  // nothing finite yet
+        const float sc = mx == -INFINITY ? 0.f : ptx::ex2((mx - gm) * kLog2e);
+        wsum *= sc;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] *= sc;
+        mx = gm;
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+            const float w = lc[k] == -INFINITY ? 0.f : ptx::ex2((lc[k] - mx) * kLog2e);
             wsum += w;
-            acc[0] = fmaf(w, v0.x, acc[0]);
-            acc[1] = fmaf(w, v0.y, acc[1]);
-            acc[2] = fmaf(w, v0.z, acc[2]);
-            acc[3] = fmaf(w, v0.w, acc[3]);
-            acc[4] = fmaf(w, v1.x, acc[4]);
-            acc[5] = fmaf(w, v1.y, acc[5]);
-            acc[6] = fmaf(w, v1.z, acc[6]);
-            acc[7] = fmaf(w, v1.w, acc[7]);
+            acc[0] = fmaf(w, v0[k].x, acc[0]);
+            acc[1] = fmaf(w, v0[k].y, acc[1]);
+            acc[2] = fmaf(w, v0[k].z, acc[2]);
+            acc[3] = fmaf(w, v0[k].w, acc[3]);
+            acc[4] = fmaf(w, v1[k].x, acc[4]);
+            acc[5] = fmaf(w, v1[k].y, acc[5]);
+            acc[6] = fmaf(w, v1[k].z, acc[6]);
+            acc[7] = fmaf(w, v1[k].w, acc[7]);
         }
     }
     const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
@@ -1035,12 +1081,15 @@ bool use_single_tile(const AttnArgs &a, int max_tail)
 // Prefix chunks (one request with a prefix).  Launch time is modelled in KV-tile iterations:
 // waves(blocks) * (tiles a block runs + kFixedTiles), where a wave is one block per SM, plus,
 // when anything is split, the merge launch and the fp32 partials written and read back
-// (bytes / kBytesPerTile).  Two forms are weighed against the unsplit launch:
+// (bytes / kBytesPerTile).  A unit runs n_pre prefix tiles and about t_est tail tiles (its row
+// pair's own span).  Cut in S chunks, chunks 0 .. S-2 take c prefix tiles each and the last one
+// the remaining n_pre - (S-1) c (0 <= that <= c) and the tail tiles, c chosen so that the longest
+// chunk is shortest.  Two forms are weighed against the unsplit launch:
 //   - every unit cut into S >= 2 chunks of c >= kMinSplitTiles tiles, within four waves (a small
 //     grid: one question against a long prefix);
 //   - whole waves of units unsplit, and only the units of the last, partial wave cut into S
-//     chunks (c >= 1 tile) that run as one more wave (e.g. 160 row-pair units on 152 SMs: 152 run
-//     whole, the other 8 in 16 one-tile chunks, instead of a second wave of 8 whole units).
+//     chunks (c >= 1 tile) that run as one more wave: they start on the SMs the whole units
+//     free first (the 2k workload: 168 units on 152 SMs, 152 whole, 16 in 6 chunks of 3 tiles).
 // A split is used when it beats the unsplit launch by at least 10 %.  (Measured: one question
 // against an 18k prefix 4x faster in 9 chunks; every unit of the 2k workload cut in 2-4 chunks
 // 5-40 % slower, which the model rejects.)
@@ -1049,7 +1098,7 @@ struct SplitPlan {
     int S, c;       // chunks per split unit and prefix tiles per chunk; S = 1: nothing split
 };
 
-SplitPlan choose_split(int64_t units, int n_pre, int d, int sms)
+SplitPlan choose_split(int64_t units, int n_pre, int t_est, int d, int sms)
 {
     constexpr int64_t kFixedTiles = 4;            // block start, pipeline fill and epilogue
     constexpr int64_t kMergeTiles = 2;            // the merge launch
@@ -1060,31 +1109,46 @@ SplitPlan choose_split(int64_t units, int n_pre, int d, int sms)
     auto partial_cost = [&](int64_t split_blocks) {  // fp32 O written and read back
         return kMergeTiles + split_blocks * (2 * BM) * d * 8 / kBytesPerTile;
     };
-    int64_t best = waves(units) * (n_pre + kFixedTiles) * 9 / 10;  // a split has to win by 10 %
-    for (int s = 2; n_pre >= 2 * kMinSplitTiles && s <= n_pre / kMinSplitTiles; ++s) {
-        const int cc = (n_pre + s - 1) / s;
-        const int ss = (n_pre + cc - 1) / cc;
-        if (ss < 2 || ss != s) continue;  // each chunk count considered once, at its own size
-        if (units * ss > 4LL * sms) break;
-        const int64_t cost = waves(units * ss) * (cc + kFixedTiles) + partial_cost(units * ss);
+    // Longest chunk (iterations) of s chunks, c >= min_c tiles each (the smallest c of the
+    // shortest); -1 if s does not fit.
+    auto chunking = [&](int s, int min_c, int &c) -> int64_t {
+        const int lo = max(min_c, (n_pre + s - 1) / s), hi = n_pre / (s - 1);
+        if (lo > hi) return -1;
+        auto len = [&](int cc) {
+            const int64_t last = static_cast<int64_t>(n_pre) - static_cast<int64_t>(s - 1) * cc + t_est;
+            return last > cc ? last : static_cast<int64_t>(cc);
+        };
+        c = min(max((n_pre + t_est + s - 1) / s, lo), hi);
+        if (c > lo && len(c - 1) <= len(c)) --c;
+        return len(c);
+    };
+    int64_t best = waves(units) * (n_pre + t_est + kFixedTiles) * 9 / 10;  // a split has to win by 10 %
+    for (int s = 2; s <= n_pre + 1 && units * s <= 4LL * sms; ++s) {
+        int c = 0;
+        const int64_t len = chunking(s, kMinSplitTiles, c);
+        if (len < 0) continue;
+        const int64_t cost = waves(units * s) * (len + kFixedTiles) + partial_cost(units * s);
         if (cost < best) {
             best = cost;
-            plan = SplitPlan{0, ss, cc};
+            plan = SplitPlan{0, s, c};
         }
     }
     const int64_t full = units / sms * sms, rest = units - full;
-    for (int s = 2; full > 0 && rest > 0 && s <= n_pre && rest * s <= sms; ++s) {
-        const int cc = (n_pre + s - 1) / s;
-        const int ss = (n_pre + cc - 1) / cc;
-        if (ss != s) continue;
-        const int64_t cost = full / sms * (n_pre + kFixedTiles) + (cc + kFixedTiles) + partial_cost(rest * ss);
+    for (int s = 2; full > 0 && rest > 0 && s <= n_pre + 1 && rest * s <= sms; ++s) {
+        int c = 0;
+        const int64_t len = chunking(s, 1, c);
+        if (len < 0) continue;
+        const int64_t cost = full / sms * (n_pre + t_est + kFixedTiles) + (len + kFixedTiles) + partial_cost(rest * s);
         if (cost < best) {
             best = cost;
-            plan = SplitPlan{full, ss, cc};
+            plan = SplitPlan{full, s, c};
         }
     }
     return plan;
 }
+
+// Tail tiles a unit is assumed to run in the split model: its row pair's own span.
+int tail_tiles_estimate(int tpt) { return (2 * tpt + BN - 1) / BN; }
 
 // Workspace after the 256-byte header when the prefix is split: partial LSE [split units][S][2 BM]
 // and partial O [split units][S][d / 4][2 BM] (fp32), each region 256-byte aligned.
@@ -1205,7 +1269,8 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
     const int64_t units = blocks * Hkv;
     int64_t whole_units = units;  // units run unsplit
     if (a.n_req == 1 && a.req_P[0] > 0) {
-        const SplitPlan plan = choose_split(units, (a.req_P[0] + BN - 1) / BN, d, sm_count_attention());
+        const SplitPlan plan = choose_split(units, (a.req_P[0] + BN - 1) / BN, tail_tiles_estimate(tpt), d,
+                                           sm_count_attention());
         if (plan.S > 1) {
             const SplitLayout lay = split_layout(units - plan.unit0, plan.S, d);
             if (ws_bytes >= lay.total) {
@@ -1247,37 +1312,43 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
         if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
         return BLINK_OK;
     }
-    // Whole units first (one block each), then the split units (n_split blocks each) and their
-    // merge.  Each block takes all 512 tensor-memory columns, so one block fits per SM (for d = 64
-    // enough shared memory is reserved to keep it so).
+    // One launch: the whole units first (one block each), then the split units (n_split blocks
+    // each), so the chunks start on the SMs the whole units free first; then the merge.  Each
+    // block takes all 512 tensor-memory columns, so one block fits per SM (for d = 64 enough
+    // shared memory is reserved to keep it so).
     const int smem = d == 128 ? Layout<128>::kAlloc : (Layout<64>::kAlloc > 120 * 1024 ? Layout<64>::kAlloc : 120 * 1024);
-    if (whole_units > 0) {
+    if (a.n_split == 1) {
         auto kern = d == 128 ? attention_kernel<128, false> : attention_kernel<64, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return BLINK_CUDA_ERROR;
-        AttnArgs aw = a;
-        aw.n_split = 1;
-        aw.split_tiles = 1 << 30;
-        kern<<<static_cast<unsigned>(whole_units), kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail,
-                                                                            tm_vtail, aw);
+        kern<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
         if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+        return BLINK_OK;
     }
-    if (a.n_split > 1) {
-        a.unit0 = static_cast<int>(whole_units);
-        const int64_t split_units = units - whole_units;
-        auto kern = d == 128 ? attention_kernel<128, true> : attention_kernel<64, true>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return BLINK_CUDA_ERROR;
-        kern<<<static_cast<unsigned>(split_units * a.n_split), kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre,
-                                                                                        tm_ktail, tm_vtail, a);
-        if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
-        const unsigned mblocks = static_cast<unsigned>(split_units * (2 * BM / kMergeRows));
-        if (d == 128)
-            split_merge_kernel<128><<<mblocks, kMergeRows * (128 / 8), 0, stream>>>(a, static_cast<int>(blocks));
-        else
-            split_merge_kernel<64><<<mblocks, kMergeRows * (64 / 8), 0, stream>>>(a, static_cast<int>(blocks));
-    }
+    a.unit0 = static_cast<int>(whole_units);
+    const int64_t split_units = units - whole_units;
+    auto kern = d == 128 ? attention_kernel<128, true> : attention_kernel<64, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return BLINK_CUDA_ERROR;
+    kern<<<static_cast<unsigned>(whole_units + split_units * a.n_split), kThreads, smem, stream>>>(
+        tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
     if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
+    // The merge as a programmatic dependent of that launch: its blocks are scheduled while the
+    // attention grid drains and start merging as soon as it ends.
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(split_units * (2 * BM / kMergeRows)));
+    cfg.blockDim = dim3(static_cast<unsigned>(kMergeRows * (d / 8)));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int nb = static_cast<int>(blocks);
+    const cudaError_t me = d == 128 ? cudaLaunchKernelEx(&cfg, split_merge_kernel<128>, a, nb)
+                                    : cudaLaunchKernelEx(&cfg, split_merge_kernel<64>, a, nb);
+    if (me != cudaSuccess || cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
     return BLINK_OK;
 }
 
@@ -1292,7 +1363,7 @@ extern "C" size_t blink_attention_workspace(int32_t rows, int32_t B, int32_t P, 
         return kHeaderBytes;
     const int tpt = BM / (Hq / Hkv);
     const int64_t blocks = ((static_cast<int64_t>(rows) + tpt - 1) / tpt + 1) / 2;
-    const SplitPlan plan = choose_split(blocks * Hkv, (P + BN - 1) / BN, d, sm_count_attention());
+    const SplitPlan plan = choose_split(blocks * Hkv, (P + BN - 1) / BN, tail_tiles_estimate(tpt), d, sm_count_attention());
     return plan.S > 1 ? split_layout(blocks * Hkv - plan.unit0, plan.S, d).total : kHeaderBytes;
 }
 

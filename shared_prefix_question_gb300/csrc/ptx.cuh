@@ -20,6 +20,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// Programmatic dependent launch (sm_90+).  A kernel launched with programmatic stream
+// serialization may be scheduled while the kernel before it in the stream still runs, once every
+// block of that kernel has executed launch_dependents (or exited); its grid_dep_wait() returns
+// when the earlier kernel has completed and its memory writes are visible.  For a kernel launched
+// without that attribute both are no-ops.  The wait ends when the earlier grid ends, and every
+// wait of that grid is bounded.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------------
