@@ -180,13 +180,15 @@ blink_status blink_kv_to_arena(const blink_bf16 *k_src, const blink_bf16 *v_src,
  *                        before its first use; the first word is the device error word
  * Prefix chunks (one request with a prefix; the work units are (row pair, kv head)): when a
  * launch-time model predicts a clear gain, units run their prefix in chunks of key tiles on
- * separate blocks whose partial outputs are merged by LSE in a further launch (the merge of the
- * prefix and tail parts, applied again).  Either every unit is cut (a small grid, e.g. a few
- * questions against a long prefix: chunks of at least 4 tiles), or whole waves of units run
- * unsplit and only the units of the last, partial wave are cut, into chunks that fill one more
- * wave.  blink_attention_workspace then includes room for the fp32 partials (it sizes them for
- * the current device); with a smaller workspace the call runs unsplit.  Results agree with the
- * unsplit path within the rounding of the merge.
+ * separate blocks whose partial outputs are merged by LSE in a second kernel (the merge of the
+ * prefix and tail parts, applied again), launched as the attention launch's programmatic
+ * dependent on `stream`.  Either every unit is cut (a small grid, e.g. a few questions against
+ * a long prefix: chunks of at least 4 tiles), or whole waves of units run unsplit and only the
+ * units of the last, partial wave are cut, into chunks that run, in the same launch, on the SMs
+ * the whole units free first.  The last chunk of a unit, which also runs its tail tiles, takes
+ * fewer prefix tiles.  blink_attention_workspace then includes room for the fp32 partials (it
+ * sizes them for the current device); with a smaller workspace the call runs unsplit.  Results
+ * agree with the unsplit path within the rounding of the merge.
  * Errors: BLINK_INVALID_ARG, BLINK_OUT_OF_RANGE, BLINK_WORKSPACE_TOO_SMALL, BLINK_CUDA_ERROR;
  * device-side: BLINK_DEVICE_FLAG (a length outside 1..max_tail or past `rows`),
  * BLINK_DEVICE_TIMEOUT.
