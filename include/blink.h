@@ -195,6 +195,19 @@ blink_status blink_kv_to_arena(const blink_bf16 *k_src, const blink_bf16 *v_src,
  * ------------------------------------------------------------------------------------------ */
 size_t blink_attention_workspace(int32_t rows, int32_t B, int32_t P, int32_t Hq, int32_t Hkv, int32_t d);
 
+/* The prefix-chunk plan blink_prefix_tail_attention uses for one request of `rows` tail rows
+ * against a prefix of P tokens, on a GPU with `sms` SMs, when the workspace has room for it (no
+ * device call: for inspection and tests).  Units are (row pair, kv head): with g = Hq / Hkv and
+ * 128 / g tokens per 128-row tile, ceil(ceil(rows / (128 / g)) / 2) * Hkv of them.
+ * *whole_units  units [0, *whole_units) run whole (all units when nothing is cut)
+ * *chunks       chunks each remaining unit is cut into (1: nothing is cut)
+ * *chunk_tiles  prefix key tiles (128 keys each) of chunks 0 .. chunks-2; the last chunk takes the
+ *               remaining 0 .. *chunk_tiles tiles and the unit's tail tiles (with *chunks = 1:
+ *               the whole prefix in tiles)
+ * Errors: BLINK_INVALID_ARG (a null output, sms < 1, or a shape the attention call rejects). */
+blink_status blink_attention_split_plan(int32_t rows, int32_t P, int32_t Hq, int32_t Hkv, int32_t d, int32_t sms,
+                                        int64_t *whole_units, int32_t *chunks, int32_t *chunk_tiles);
+
 blink_status blink_prefix_tail_attention(const blink_bf16 *q, const blink_bf16 *k_pre, const blink_bf16 *v_pre,
                                          int64_t pre_row_stride, const blink_bf16 *k_tail,
                                          const blink_bf16 *v_tail, const int32_t *d_cu_seqlens,

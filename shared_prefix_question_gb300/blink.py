@@ -50,6 +50,7 @@ _SIGNATURES = {
     "blink_pack_plan_workspace": (_sz, [_i32]),
     "blink_pack_plan": (_i32, [_vp, _i32, _i32, _i32] + [_vp] * 10 + [_vp]),
     "blink_attention_workspace": (_sz, [_i32] * 6),
+    "blink_attention_split_plan": (_i32, [_i32] * 6 + [_vp] * 3),
     "blink_prefix_tail_attention": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                            _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp]),
     "blink_prefix_tail_attention_multi": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp,
@@ -149,6 +150,16 @@ def pack_plan_workspace_bytes(n: int) -> int:
 
 def attention_workspace_bytes(rows, B, P, Hq, Hkv, d) -> int:
     return int(lib().blink_attention_workspace(rows, B, P, Hq, Hkv, d))
+
+
+def blink_attention_split_plan(rows: int, P: int, Hq: int, Hkv: int, d: int, sms: int):
+    """The prefix-chunk plan of one request on a GPU with `sms` SMs (host computation only):
+    (whole_units, chunks, chunk_tiles) as include/blink.h describes them."""
+    w, c, t = ctypes.c_int64(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    st = lib().blink_attention_split_plan(int(rows), int(P), int(Hq), int(Hkv), int(d), int(sms), ctypes.byref(w),
+                                          ctypes.byref(c), ctypes.byref(t))
+    _check(st, "blink_attention_split_plan")
+    return int(w.value), int(c.value), int(t.value)
 
 
 def new_workspace(nbytes: int, device) -> torch.Tensor:

@@ -1367,6 +1367,25 @@ extern "C" size_t blink_attention_workspace(int32_t rows, int32_t B, int32_t P, 
     return plan.S > 1 ? split_layout(blocks * Hkv - plan.unit0, plan.S, d).total : kHeaderBytes;
 }
 
+extern "C" blink_status blink_attention_split_plan(int32_t rows, int32_t P, int32_t Hq, int32_t Hkv, int32_t d,
+                                                  int32_t sms, int64_t *whole_units, int32_t *chunks,
+                                                  int32_t *chunk_tiles)
+{
+    using namespace blink;
+    if (!whole_units || !chunks || !chunk_tiles) return BLINK_INVALID_ARG;
+    if (rows < 1 || P < 0 || P > BLINK_MAX_INPUT_TOKENS || Hq < 1 || Hkv < 1 || Hkv > 65535 || Hq % Hkv != 0 ||
+        (d != 64 && d != 128) || Hq / Hkv > BM || sms < 1)
+        return BLINK_INVALID_ARG;
+    const int tpt = BM / (Hq / Hkv);
+    const int64_t units = ((static_cast<int64_t>(rows) + tpt - 1) / tpt + 1) / 2 * Hkv;
+    const int n_pre = (P + BN - 1) / BN;
+    const SplitPlan plan = P > 0 ? choose_split(units, n_pre, tail_tiles_estimate(tpt), d, sms) : SplitPlan{units, 1, 0};
+    *whole_units = plan.S > 1 ? plan.unit0 : units;
+    *chunks = plan.S;
+    *chunk_tiles = plan.S > 1 ? plan.c : n_pre;
+    return BLINK_OK;
+}
+
 extern "C" blink_status blink_prefix_tail_attention(const blink_bf16 *q, const blink_bf16 *k_pre,
                                                     const blink_bf16 *v_pre, int64_t pre_row_stride,
                                                     const blink_bf16 *k_tail, const blink_bf16 *v_tail,

@@ -303,3 +303,23 @@ def test_attention_split_of_the_last_partial_wave(case):
             owned[s0:s0 + L] = True
         assert (out[~owned] == 0).all()
         assert np.isneginf(lse[:, ~owned]).all()
+
+
+@pytest.mark.gpu
+def test_workspace_query_holds_the_split_plan():
+    """blink_attention_workspace sizes the fp32 partials of exactly the plan blink_attention_split_plan
+    reports for this GPU's SM count (256-byte header, then LSE and O of every chunk of every cut
+    unit, each region 256-byte aligned)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for rows, P, Hq, Hkv, d in [(1306, 2048, 32, 8, 128), (128, 18432, 32, 8, 128), (64, 18432, 32, 8, 128),
+                                (40, 4096, 8, 2, 128), (144, 3000, 10, 2, 64), (10627, 18432, 32, 8, 128)]:
+        whole, S, c = blink.blink_attention_split_plan(rows, P, Hq, Hkv, d, sms)
+        ws = blink.attention_workspace_bytes(rows, 1, P, Hq, Hkv, d)
+        if S == 1:
+            assert ws == 256
+            continue
+        tpt = 128 // (Hq // Hkv)
+        units = (-(-rows // tpt) + 1) // 2 * Hkv
+        n = (units - whole) * S
+        up = lambda x: -(-x // 256) * 256
+        assert ws == 256 + up(n * 256 * 4) + up(n * 256 * d * 4)
