@@ -29,8 +29,9 @@
 // its own sum) and LSE in fp32, the last chunk also runs the tail tiles, and split_merge_kernel
 // combines the chunks by LSE -- the same merge that joins the prefix and tail parts.  The whole
 // units and the chunks run in one launch (whole units first, so a chunk starts on the first SM
-// that frees up); the chunked form is a separate instantiation (kSplit), so the common unsplit
-// kernel carries none of it.
+// that frees up).  The forms are separate instantiations (kMode: whole units only, whole units
+// then chunks, chunks only), so the common unsplit kernel carries none of the chunk code and a
+// launch of chunks only carries none of the whole-unit epilogue.
 #include <cstdint>
 
 #include "common.cuh"
@@ -157,9 +158,10 @@ __device__ __forceinline__ bool question_ok(const AttnArgs &a, int s, int L)
     return L >= 1 && L <= a.max_tail && s >= 0 && static_cast<long long>(s) + L <= a.rows;
 }
 
-// kSplit: this launch runs prefix chunks (n_split > 1) after its whole units and writes their
-// partial results; without it the chunk arithmetic folds away and the kernel is the plain one.
-template <int D, bool kSplit>
+// kMode 0: whole units only (the chunk arithmetic folds away: the plain kernel); 1: whole units,
+// then prefix chunks (n_split > 1) that write partial results; 2: prefix chunks only.
+constexpr int kWholeUnits = 0, kUnitsThenChunks = 1, kChunksOnly = 2;
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kpre,
                      const __grid_constant__ CUtensorMap tm_vpre, const __grid_constant__ CUtensorMap tm_ktail,
@@ -186,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int bid = static_cast<int>(blockIdx.x);
-    const bool chunk = kSplit && bid >= a.unit0;                     // a prefix chunk, not a whole unit
+    constexpr bool kSplit = kMode != kWholeUnits;
+    const bool chunk = kMode == kChunksOnly || (kMode == kUnitsThenChunks && bid >= a.unit0);  // not a whole unit
     const int local = chunk ? (bid - a.unit0) / a.n_split : 0;       // split unit
     const int split = chunk ? (bid - a.unit0) % a.n_split : 0;       // prefix chunk
     const int unit = chunk ? a.unit0 + local : bid;
@@ -1318,7 +1321,7 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
     // shared memory is reserved to keep it so).
     const int smem = d == 128 ? Layout<128>::kAlloc : (Layout<64>::kAlloc > 120 * 1024 ? Layout<64>::kAlloc : 120 * 1024);
     if (a.n_split == 1) {
-        auto kern = d == 128 ? attention_kernel<128, false> : attention_kernel<64, false>;
+        auto kern = d == 128 ? attention_kernel<128, kWholeUnits> : attention_kernel<64, kWholeUnits>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return BLINK_CUDA_ERROR;
         kern<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(tm_q, tm_kpre, tm_vpre, tm_ktail, tm_vtail, a);
@@ -1327,7 +1330,9 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
     }
     a.unit0 = static_cast<int>(whole_units);
     const int64_t split_units = units - whole_units;
-    auto kern = d == 128 ? attention_kernel<128, true> : attention_kernel<64, true>;
+    auto kern = whole_units > 0
+                    ? (d == 128 ? attention_kernel<128, kUnitsThenChunks> : attention_kernel<64, kUnitsThenChunks>)
+                    : (d == 128 ? attention_kernel<128, kChunksOnly> : attention_kernel<64, kChunksOnly>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BLINK_CUDA_ERROR;
     kern<<<static_cast<unsigned>(whole_units + split_units * a.n_split), kThreads, smem, stream>>>(
