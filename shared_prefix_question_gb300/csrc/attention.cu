@@ -158,6 +158,56 @@ __device__ __forceinline__ bool question_ok(const AttnArgs &a, int s, int L)
     return L >= 1 && L <= a.max_tail && s >= 0 && static_cast<long long>(s) + L <= a.rows;
 }
 
+// Masks for the tail tiles.  Keys [J0, J0 + 32) of a row are set to -inf where key < lo or
+// key > hi (the row's question start and its own token, relative to the tile).  A 32-key chunk
+// that every row of the warp keeps whole is left alone and one that every row drops is cleared,
+// so only the chunk a boundary crosses is masked key by key: on a causal diagonal tile that is one
+// chunk in four.  The per-key step is written out in PTX (a compare, a compare-or, a predicated
+// move of -inf per key) so that the row's 128 scores stay in registers across the branches (the
+// same branches in C++ cost 2.4 KB of spills).
+#define BLINK_MASK1(k) \
+    "setp.gt.s32 p, %32, " #k "; setp.lt.or.s32 p, %33, " #k ", p; @p mov.f32 %" #k ", 0fFF800000;\n\t"
+#define BLINK_DROP1(k) "mov.f32 %" #k ", 0fFF800000;\n\t"
+#define BLINK_X8(M, a, b, c, d, e, f, g, h) M(a) M(b) M(c) M(d) M(e) M(f) M(g) M(h)
+#define BLINK_X32(M)                                                                                           \
+    BLINK_X8(M, 0, 1, 2, 3, 4, 5, 6, 7)                                                                        \
+    BLINK_X8(M, 8, 9, 10, 11, 12, 13, 14, 15)                                                                  \
+    BLINK_X8(M, 16, 17, 18, 19, 20, 21, 22, 23) BLINK_X8(M, 24, 25, 26, 27, 28, 29, 30, 31)
+#define BLINK_OPS32(J)                                                                                          \
+    "+f"(s[J + 0]), "+f"(s[J + 1]), "+f"(s[J + 2]), "+f"(s[J + 3]), "+f"(s[J + 4]), "+f"(s[J + 5]),             \
+        "+f"(s[J + 6]), "+f"(s[J + 7]), "+f"(s[J + 8]), "+f"(s[J + 9]), "+f"(s[J + 10]), "+f"(s[J + 11]),       \
+        "+f"(s[J + 12]), "+f"(s[J + 13]), "+f"(s[J + 14]), "+f"(s[J + 15]), "+f"(s[J + 16]), "+f"(s[J + 17]),   \
+        "+f"(s[J + 18]), "+f"(s[J + 19]), "+f"(s[J + 20]), "+f"(s[J + 21]), "+f"(s[J + 22]), "+f"(s[J + 23]),   \
+        "+f"(s[J + 24]), "+f"(s[J + 25]), "+f"(s[J + 26]), "+f"(s[J + 27]), "+f"(s[J + 28]), "+f"(s[J + 29]),   \
+        "+f"(s[J + 30]), "+f"(s[J + 31])
+
+template <int J0>
+__device__ __forceinline__ void mask_chunk(float (&s)[BN], int lo, int hi)
+{
+    if (__all_sync(0xFFFFFFFFu, lo <= J0 && hi >= J0 + 31)) return;
+    if (__all_sync(0xFFFFFFFFu, hi < J0 || lo > J0 + 31)) {
+        asm volatile("{\n\t" BLINK_X32(BLINK_DROP1) "}" : BLINK_OPS32(J0));
+    } else {
+        const int dlo = lo - J0, dhi = hi - J0;  // key k of the chunk is dropped if k < dlo or k > dhi
+        asm volatile("{\n\t.reg .pred p;\n\t" BLINK_X32(BLINK_MASK1) "}" : BLINK_OPS32(J0) : "r"(dlo), "r"(dhi));
+    }
+}
+
+// Every tail-tile mask of a row: its keys below lo or above hi.
+__device__ __forceinline__ void mask_tail_tile(float (&s)[BN], int lo, int hi)
+{
+    if (__all_sync(0xFFFFFFFFu, lo <= 0 && hi >= BN - 1)) return;  // most tiles of a long causal tail
+    mask_chunk<0>(s, lo, hi);
+    mask_chunk<32>(s, lo, hi);
+    mask_chunk<64>(s, lo, hi);
+    mask_chunk<96>(s, lo, hi);
+}
+#undef BLINK_MASK1
+#undef BLINK_DROP1
+#undef BLINK_X8
+#undef BLINK_X32
+#undef BLINK_OPS32
+
 // kMode 0: whole units only (the chunk arithmetic folds away: the plain kernel); 1: whole units,
 // then prefix chunks (n_split > 1) that write partial results; 2: prefix chunks only.
 constexpr int kWholeUnits = 0, kUnitsThenChunks = 1, kChunksOnly = 2;
@@ -496,12 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb = kbeg + (i - n_pre) * BN;
                 const int lo_j = q_lo - kb;
                 const int hi_j = owned ? tok - kb : -1;
-                // tiles every row of the warp sees whole (most of a long causal tail) need no mask
-                if (!__all_sync(0xFFFFFFFFu, lo_j <= 0 && hi_j >= BN - 1)) {
-#pragma unroll
-                    for (int j = 0; j < BN; ++j)
-                        if (j < lo_j || j > hi_j) s[j] = -INFINITY;
-                }
+                mask_tail_tile(s, lo_j, hi_j);
             }
             // row max, three operands per instruction, four independent chains
             float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
@@ -881,11 +926,7 @@ __global__ void __launch_bounds__(kThreads1, 2)
                 const int kb = kbeg + (i - n_pre) * BN;
                 const int lo_j = q_lo - kb;
                 const int hi_j = owned ? tok - kb : -1;
-                if (!__all_sync(0xFFFFFFFFu, lo_j <= 0 && hi_j >= BN - 1)) {
-#pragma unroll
-                    for (int j = 0; j < BN; ++j)
-                        if (j < lo_j || j > hi_j) s[j] = -INFINITY;
-                }
+                mask_tail_tile(s, lo_j, hi_j);
             }
             float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
