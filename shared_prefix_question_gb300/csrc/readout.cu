@@ -15,6 +15,7 @@
 
 #include "answer.cuh"
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace blink {
 namespace {
@@ -131,6 +132,9 @@ __global__ void __launch_bounds__(kReadoutWarps * 32, 6)
 {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // readout_finish_kernel is launched as this kernel's programmatic dependent: it may be
+    // scheduled once every block has started, and waits for this grid's end before it reads.
+    if constexpr (!kFused) ptx::grid_launch_dependents();
 
     // Distributed check of the CSR offsets: block c checks questions c, c + grid, ...
     for (int b = blockIdx.x * blockDim.x + threadIdx.x; b <= B; b += gridDim.x * blockDim.x) {
@@ -214,12 +218,32 @@ __global__ void __launch_bounds__(kReadoutWarps * 32)
                           float *__restrict__ probs, const int32_t *__restrict__ qtype, float *__restrict__ answers,
                           int *__restrict__ err)
 {
+    ptx::grid_dep_wait();  // the logits of readout_kernel<false>, launched just before
     const int b = blockIdx.x * kReadoutWarps + (threadIdx.x >> 5);
     if (b >= B) return;
     const int lo = max(0, min(sum_k, __ldg(label_off + b)));
     const int hi = max(lo, min(sum_k, __ldg(label_off + b + 1)));
     if (hi - lo < 1 || hi - lo > BLINK_MAX_OPTIONS) return;  // flagged by the offsets check
     finish_question(b, lo, hi, threadIdx.x & 31, log2e_over_t, probs, qtype, answers, err);
+}
+
+// readout_finish_kernel as the programmatic dependent of the readout_kernel<false> launch just
+// before it on `stream`: its blocks are scheduled while the logit launch drains.
+cudaError_t launch_finish(const int32_t *label_off, int B, int sum_k, float log2e_over_t, float *probs,
+                          const int32_t *qtype, float *answers, int *err, cudaStream_t stream)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((B + kReadoutWarps - 1) / kReadoutWarps));
+    cfg.blockDim = dim3(kReadoutWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, readout_finish_kernel, label_off, B, sum_k, log2e_over_t, probs, qtype, answers,
+                              err);
 }
 
 }  // namespace
@@ -261,8 +285,9 @@ extern "C" blink_status blink_label_readout(const blink_bf16 *hidden, int64_t hi
             hidden, hidden_row_stride, hidden_rows, d_last_idx, d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
             sum_k, log2e_over_t, d_probs, d_logits, d_qtype, d_answers, counters, &hdr->error);
         if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
-        readout_finish_kernel<<<(B + kReadoutWarps - 1) / kReadoutWarps, kReadoutWarps * 32, 0, stream>>>(
-            d_label_off, B, sum_k, log2e_over_t, d_probs, d_qtype, d_answers, &hdr->error);
+        if (launch_finish(d_label_off, B, sum_k, log2e_over_t, d_probs, d_qtype, d_answers, &hdr->error, stream) !=
+            cudaSuccess)
+            return BLINK_CUDA_ERROR;
     } else {
         if (cudaMemsetAsync(counters, 0, static_cast<size_t>(B) * sizeof(uint32_t), stream) != cudaSuccess)
             return BLINK_CUDA_ERROR;
@@ -386,8 +411,8 @@ extern "C" blink_status blink_label_readout_noalloc(const blink_bf16 *hidden, in
             hidden, hidden_row_stride, hidden_rows, d_last_idx, d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
             sum_k, log2e_over_t, d_probs, d_logits, nullptr, nullptr, counters, err);
         if (cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
-        readout_finish_kernel<<<(B + kReadoutWarps - 1) / kReadoutWarps, kReadoutWarps * 32, 0, stream>>>(
-            d_label_off, B, sum_k, log2e_over_t, d_probs, nullptr, nullptr, err);
+        if (launch_finish(d_label_off, B, sum_k, log2e_over_t, d_probs, nullptr, nullptr, err, stream) != cudaSuccess)
+            return BLINK_CUDA_ERROR;
     } else {
         readout_kernel<true><<<grid, kReadoutWarps * 32, 0, stream>>>(
             hidden, hidden_row_stride, hidden_rows, d_last_idx, d_slot_of, unembed, V, H, d_label_off, d_label_ids, B,
