@@ -1028,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads1, 2)
 // visibility of its partials) before it reads anything.
 constexpr int kMergeRows = 16;  // rows per merge block
 
-template <int D>
+template <int D, int kGroup>
 __global__ void __launch_bounds__(kMergeRows * (D / 8))
     split_merge_kernel(const AttnArgs a, int nb)
 {
@@ -1045,10 +1045,10 @@ __global__ void __launch_bounds__(kMergeRows * (D / 8))
     if (r >= a.g * a.tpt || tok >= a.rows) return;
     const int S = a.n_split;
     const int64_t row0 = static_cast<int64_t>(local) * S * (2 * BM) + rr;
-    // One pass over the chunks in groups of eight: a group's LSE and O loads are all issued before
-    // any is used (one L2 round trip per group), and the running sums are rescaled to each new
-    // maximum, so the weights are exp(lse_c - max) with max over all chunks, as above.
-    constexpr int kGroup = 8;
+    // One pass over the chunks in groups of kGroup: a group's LSE and O loads are all issued
+    // before any is used (one L2 round trip per group), and the running sums are rescaled to each
+    // new maximum, so the weights are exp(lse_c - max) with max over all chunks, as above.  (Groups
+    // of 8 take 103 registers, of 12 139: the wider form only where it saves a round trip.)
     float mx = -INFINITY, wsum = 0.f, acc[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[k] = 0.f;
@@ -1392,8 +1392,10 @@ blink_status launch_attention(AttnArgs &a, const blink_bf16 *q, const blink_bf16
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const int nb = static_cast<int>(blocks);
-    const cudaError_t me = d == 128 ? cudaLaunchKernelEx(&cfg, split_merge_kernel<128>, a, nb)
-                                    : cudaLaunchKernelEx(&cfg, split_merge_kernel<64>, a, nb);
+    const bool wide = a.n_split > 8;  // 9-12 chunks in one round trip, 13-24 in two
+    const cudaError_t me =
+        d == 128 ? cudaLaunchKernelEx(&cfg, wide ? split_merge_kernel<128, 12> : split_merge_kernel<128, 8>, a, nb)
+                 : cudaLaunchKernelEx(&cfg, wide ? split_merge_kernel<64, 12> : split_merge_kernel<64, 8>, a, nb);
     if (me != cudaSuccess || cudaGetLastError() != cudaSuccess) return BLINK_CUDA_ERROR;
     return BLINK_OK;
 }
